@@ -1,0 +1,353 @@
+"""CPU oracle for the fused NVFP4 activation producers (test infrastructure).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg import
+this package.  The library never does: the CUDA path fails loudly when its
+extension is missing and has no CPU fallback.
+
+The arithmetic lives in ``h3q_oracle.c`` (plain C, binary32, one rounding per
+operation, built with ``-ffp-contract=off``).  This module compiles it with
+gcc on first use and wraps it for numpy arrays.  bf16 tensors travel as
+``uint16`` arrays of their bit patterns.
+
+Functions here mirror the four library calls on host arrays:
+
+* :func:`quantize_rows`  -- standalone NVFP4 quantize (attention output)
+* :func:`adaln_rows`     -- RMSNorm (fp32 statistics) + AdaLN modulation -> NVFP4
+* :func:`swiglu_rows`    -- silu(gate) * up -> NVFP4
+* :func:`dequantize_rows`-- codes + block scales -> fp32
+
+plus :func:`swizzle_scales` (logical [rows, cols/16] scales to the 128x4
+layout with zeroed padding rows) and the element-wise conversions the pin
+tests check.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "h3q_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (host compiler)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if force or not fresh:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+
+_SIGNATURES = {
+    "orc_bf16_bits": ([_F], ctypes.c_uint16),
+    "orc_bf16_value": ([ctypes.c_uint16], _F),
+    "orc_e4m3_value": ([ctypes.c_uint8], _F),
+    "orc_e4m3_encode": ([_F], ctypes.c_uint8),
+    "orc_e2m1_value": ([ctypes.c_uint8], _F),
+    "orc_e2m1_encode": ([_F], ctypes.c_uint8),
+    "orc_exp": ([_F], _F),
+    "orc_exp_constants": ([_P], None),
+    "orc_swiglu_value": ([_F, _F], _F),
+    "orc_quantize_block": ([_P, _F, _P, _P], None),
+    "orc_global_scale": ([_F], _F),
+    "orc_scale_offset": ([_I64, _I64, _I64], _I64),
+    "orc_padded_rows": ([_I64], _I64),
+    "orc_swizzle_scales": ([_P, _I64, _I64, _P], None),
+    "orc_quantize_rows": ([_P, _I64, _I64, _I64, _F, _P, _P, _P], None),
+    "orc_row_rstd": ([_P, _I64, _F], _F),
+    "orc_adaln_rows": ([_P, _I64, _I64, _I64, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P], None),
+    "orc_swiglu_rows": ([_P, _I64, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P], None),
+    "orc_dequantize_rows": ([_P, _P, _I64, _I64, _F, _P], None),
+    "orc_bf16_bits_array": ([_P, _I64, _P], None),
+    "orc_e4m3_encode_array": ([_P, _I64, _P], None),
+    "orc_e2m1_encode_array": ([_P, _I64, _P], None),
+    "orc_exp_array": ([_P, _I64, _P], None),
+    "orc_swiglu_value_array": ([_P, _P, _I64, _P], None),
+}
+
+
+def lib():
+    """The loaded oracle library (built on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            handle = ctypes.CDLL(build())
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 data must be passed as uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _check_cols(cols: int) -> None:
+    if cols <= 0 or cols % 64:
+        raise ValueError(f"cols must be a positive multiple of 64, got {cols}")
+
+
+def _split(n: int, threads: int):
+    threads = max(1, min(threads, n))
+    step = (n + threads - 1) // threads
+    return [(s, min(n, s + step)) for s in range(0, n, step)]
+
+
+# --------------------------------------------------------------------------- #
+# element-wise conversions (used by the pins)                                  #
+# --------------------------------------------------------------------------- #
+
+def bf16_bits(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_bf16_bits_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    bits = _u16(bits)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().orc_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    return lib().orc_e4m3_value(code)
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().orc_e2m1_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(code)
+
+
+def exp_c(z: np.ndarray) -> np.ndarray:
+    z = np.ascontiguousarray(z, dtype=np.float32)
+    out = np.empty(z.shape, np.float32)
+    lib().orc_exp_array(_ptr(z), z.size, _ptr(out))
+    return out
+
+
+def exp_constants() -> dict:
+    buf = np.zeros(11, np.float32)
+    lib().orc_exp_constants(_ptr(buf))
+    names = ["L2E", "C1", "C2"] + [f"P{n}" for n in range(8)]
+    return dict(zip(names, buf.tolist()))
+
+
+def swiglu_value(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(gate, dtype=np.float32)
+    u = np.ascontiguousarray(up, dtype=np.float32)
+    assert g.shape == u.shape
+    out = np.empty(g.shape, np.float32)
+    lib().orc_swiglu_value_array(_ptr(g), _ptr(u), g.size, _ptr(out))
+    return out
+
+
+def quantize_block(y, gsf: float):
+    """(scale byte, 8 packed code bytes) of one 16-element block of fp32 values."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    assert y.shape == (16,)
+    sf = np.zeros(1, np.uint8)
+    packed = np.zeros(8, np.uint8)
+    lib().orc_quantize_block(_ptr(y), float(gsf), _ptr(sf), _ptr(packed))
+    return int(sf[0]), packed
+
+
+def global_scale(amax: float) -> float:
+    """fl(448 * 6 / amax): the static per-tensor scale for a tensor amax."""
+    if not amax > 0:
+        raise ValueError("global amax must be positive")
+    return float(lib().orc_global_scale(float(amax)))
+
+
+# --------------------------------------------------------------------------- #
+# layout                                                                        #
+# --------------------------------------------------------------------------- #
+
+def padded_rows(rows: int) -> int:
+    return int(lib().orc_padded_rows(rows))
+
+
+def scale_offset(row: int, group: int, cols: int) -> int:
+    return int(lib().orc_scale_offset(row, group, cols))
+
+
+def scale_offsets(rows: np.ndarray, cols: int) -> np.ndarray:
+    """[len(rows), cols/16] int64 swizzled offsets of the scales of the given rows."""
+    rows = np.asarray(rows, dtype=np.int64)
+    groups = cols // 16
+    out = np.empty((rows.size, groups), np.int64)
+    f = lib().orc_scale_offset
+    for i, r in enumerate(rows.tolist()):
+        for g in range(groups):
+            out[i, g] = f(r, g, cols)
+    return out
+
+
+def swizzle_scales(sf_logical: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    _check_cols(cols)
+    sf = np.ascontiguousarray(sf_logical, dtype=np.uint8)
+    assert sf.shape == (rows, cols // 16)
+    out = np.empty(padded_rows(rows) * (cols // 16), np.uint8)
+    lib().orc_swizzle_scales(_ptr(sf), rows, cols, _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# row producers                                                                 #
+# --------------------------------------------------------------------------- #
+
+def quantize_rows(x_bits: np.ndarray, gsf: float, threads: int = 1):
+    """Standalone quantize of bf16 rows [n, cols] -> (codes [n, cols/2], sf [n, cols/16])."""
+    x = _u16(x_bits)
+    n, cols = x.shape
+    _check_cols(cols)
+    codes = np.empty((n, cols // 2), np.uint8)
+    sf = np.empty((n, cols // 16), np.uint8)
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(cols, np.float32)
+        lib().orc_quantize_rows(_ptr(x[a:b]), b - a, cols, cols, float(gsf), _ptr(scratch),
+                                _ptr(codes[a:b]), _ptr(sf[a:b]))
+
+    _run(work, n, threads)
+    return codes, sf
+
+
+def row_rstd(x_row_bits: np.ndarray, eps: float) -> float:
+    x = _u16(x_row_bits)
+    _check_cols(x.size)
+    return float(lib().orc_row_rstd(_ptr(x), x.size, float(eps)))
+
+
+def adaln_rows(x_bits, gamma_bits, table_bits, frames, eps: float, gsf: float | None,
+               want_y: bool = False, threads: int = 1):
+    """RMSNorm + AdaLN -> NVFP4 of bf16 rows [n, cols].
+
+    ``table_bits`` is [T, 2, cols] (index 0 shift, 1 scale); ``frames[i]`` is
+    the frame of row i.  With ``gsf=None`` only rstd (and y) are produced.
+    Returns (codes, sf, rstd, y) with y (bf16 bits) or None.
+    """
+    x = _u16(x_bits)
+    n, cols = x.shape
+    _check_cols(cols)
+    gamma = _u16(gamma_bits).reshape(cols)
+    table = _u16(table_bits)
+    assert table.ndim == 3 and table.shape[1:] == (2, cols)
+    frames = np.ascontiguousarray(frames, dtype=np.int64).reshape(n)
+    if n and (frames.min() < 0 or frames.max() >= table.shape[0]):
+        raise ValueError("frame index outside [0, frames)")
+    quant = gsf is not None
+    codes = np.empty((n, cols // 2), np.uint8) if quant else None
+    sf = np.empty((n, cols // 16), np.uint8) if quant else None
+    rstd = np.empty(n, np.float32)
+    y = np.empty((n, cols), np.uint16) if want_y else None
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(cols, np.float32)
+        lib().orc_adaln_rows(_ptr(x[a:b]), b - a, cols, cols, _ptr(gamma), _ptr(table),
+                             _ptr(frames[a:b]), float(eps), float(gsf if quant else 1.0),
+                             _ptr(scratch), _ptr(codes[a:b]) if quant else None,
+                             _ptr(sf[a:b]) if quant else None, _ptr(rstd[a:b]),
+                             _ptr(y[a:b]) if want_y else None)
+
+    _run(work, n, threads)
+    return codes, sf, rstd, y
+
+
+def swiglu_rows(gate_bits, up_bits, gsf: float | None, want_y: bool = False, threads: int = 1):
+    """silu(gate) * up -> NVFP4 of bf16 rows [n, cols]. Returns (codes, sf, y)."""
+    g = _u16(gate_bits)
+    u = _u16(up_bits)
+    assert g.shape == u.shape
+    n, cols = g.shape
+    _check_cols(cols)
+    quant = gsf is not None
+    codes = np.empty((n, cols // 2), np.uint8) if quant else None
+    sf = np.empty((n, cols // 16), np.uint8) if quant else None
+    y = np.empty((n, cols), np.uint16) if want_y else None
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(cols, np.float32)
+        lib().orc_swiglu_rows(_ptr(g[a:b]), cols, _ptr(u[a:b]), cols, b - a, cols,
+                              float(gsf if quant else 1.0), _ptr(scratch),
+                              _ptr(codes[a:b]) if quant else None,
+                              _ptr(sf[a:b]) if quant else None,
+                              _ptr(y[a:b]) if want_y else None)
+
+    _run(work, n, threads)
+    return codes, sf, y
+
+
+def dequantize_rows(codes: np.ndarray, sf_logical: np.ndarray, gsf: float,
+                    threads: int = 1) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf_logical, dtype=np.uint8)
+    n, half = codes.shape
+    cols = 2 * half
+    _check_cols(cols)
+    assert sf.shape == (n, cols // 16)
+    out = np.empty((n, cols), np.float32)
+
+    def work(span):
+        a, b = span
+        lib().orc_dequantize_rows(_ptr(codes[a:b]), _ptr(sf[a:b]), b - a, cols, float(gsf),
+                                  _ptr(out[a:b]))
+
+    _run(work, n, threads)
+    return out
+
+
+def _run(work, n: int, threads: int) -> None:
+    if n == 0:
+        return
+    spans = _split(n, threads)
+    if len(spans) == 1:
+        work(spans[0])
+        return
+    # ctypes releases the GIL during the C call, so row spans run in parallel.
+    with ThreadPoolExecutor(len(spans)) as pool:
+        list(pool.map(work, spans))
