@@ -1,0 +1,531 @@
+"""Throughput of the fused NVFP4 activation producers on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of the fused RMSNorm + AdaLN -> NVFP4 producer over the
+65,280 x 7,168 bf16 workload (32 frames x 2,040 tokens, the MiniMax-H3 video
+DiT shape).  The headline is HBM GB/s: the algorithmic bytes of a call (bf16
+input read once, codes and swizzled scales written once, gamma and the
+modulation table read once) over the call's device time.  The input (936 MB)
+is larger than L2, so nothing is flushed between steps.
+
+Printed as one JSON line on rank 0, with:
+  roofline     the producer kernel against the measured HBM copy bandwidth,
+               and its DRAM traffic per launch from the committed ncu summary
+  cpu_baseline the CPU oracle on the host cores over a bounded sample
+  e2e          the same metric through the public call with host buffers:
+               pinned host -> device copy of the step's inputs, the call, and
+               device -> host copy of its codes and scales, all timed
+  producers    the other producers measured the same way (SwiGLU, the
+               standalone quantize, the attention-output quantize)
+  clocks       nvidia-smi samples taken while the kernels ran
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (the rows
+are independent and the global scale is static, so no data moves between
+ranks); the time is the maximum over ranks and the value counts all ranks'
+bytes.  ``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "fused RMSNorm+AdaLN→NVFP4 HBM GB/s (% of GB300 peak) at 65,280×7,168 bf16"
+ROWS, COLS = workloads.TOKENS, workloads.HIDDEN
+FRAMES, RPF = workloads.FRAMES, workloads.TOKENS_PER_FRAME
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+# --------------------------------------------------------------------------- #
+# bytes and peaks                                                               #
+# --------------------------------------------------------------------------- #
+
+def padded(rows: int) -> int:
+    return (rows + 127) // 128 * 128
+
+
+def out_bytes(rows: int, cols: int) -> int:
+    return rows * cols // 2 + padded(rows) * cols // 16
+
+
+def adaln_bytes(rows: int, cols: int, frames: int) -> int:
+    # x read + codes + scales written + gamma + modulation table + global scale
+    return 2 * rows * cols + out_bytes(rows, cols) + 2 * cols + frames * 2 * cols * 2 + 4
+
+
+def quantize_bytes(rows: int, cols: int) -> int:
+    return 2 * rows * cols + out_bytes(rows, cols) + 4
+
+
+def swiglu_bytes(rows: int, cols: int) -> int:
+    return 4 * rows * cols + out_bytes(rows, cols) + 4
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "nvfp4_activation_quantize_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from profiles/dram_traffic.txt, if they were
+    taken from the current kernel sources (lines: kernel source-hash bytes note)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
+                return int(parts[2]) if parts[1] == want else None
+    return None
+
+
+# --------------------------------------------------------------------------- #
+# clocks                                                                        #
+# --------------------------------------------------------------------------- #
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while kernels run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._reader.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if not (t0 <= t <= t1):
+                continue
+            f = [p.strip() for p in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() in ("active", "0x1", "1"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# timing helpers                                                                #
+# --------------------------------------------------------------------------- #
+
+def time_launches(fn, steps: int, stream, flush=None):
+    """Run fn() `steps` times on `stream`, each bracketed by its own CUDA events.
+    Returns (total_ms from the first start to the last end, per-launch ms list)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            if flush is not None:
+                flush()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return starts[0].elapsed_time(ends[-1]), per
+
+
+def calibrate_adaln_gsf(w) -> float:
+    """Global scale from max |modulated x| (torch fp32 on the GPU, a calibration
+    pass outside the timed region)."""
+    x, gamma, table = w["x"], w["gamma"].float(), w["table"].float()
+    amax = 0.0
+    step = 4096
+    for r0 in range(0, x.shape[0], step):
+        xf = x[r0:r0 + step].float()
+        rstd = torch.rsqrt(xf.pow(2).mean(1, keepdim=True) + w["eps"])
+        t = torch.arange(r0, r0 + xf.shape[0], device=x.device) // w["rows_per_frame"]
+        y = xf * rstd * gamma * (1 + table[t, 1]) + table[t, 0]
+        amax = max(amax, float(y.abs().max()))
+    return 2688.0 / amax
+
+
+def calibrate_swiglu_gsf(gate, up) -> float:
+    amax = 0.0
+    for r0 in range(0, gate.shape[0], 4096):
+        g = gate[r0:r0 + 4096].float()
+        y = torch.nn.functional.silu(g) * up[r0:r0 + 4096].float()
+        amax = max(amax, float(y.abs().max()))
+    return 2688.0 / amax
+
+
+# --------------------------------------------------------------------------- #
+# our arm                                                                       #
+# --------------------------------------------------------------------------- #
+
+def run_ours(args, rank, world, dev):
+    import nvfp4_activation_quantize_gb300 as h3q
+
+    h3q.library()
+    stream = torch.cuda.current_stream(dev)
+    w = workloads.adaln_inputs(dev)
+    gsf_val = calibrate_adaln_gsf(w)
+    gsf = torch.tensor([gsf_val], dtype=torch.float32, device=dev)
+    codes = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], gsf, rows_per_frame=RPF,
+                                    eps=w["eps"], codes=codes, scales=scales, stream=stream)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    # keep the GPU busy long enough for the clock samples (untimed)
+    torch.cuda.synchronize()
+    soak_t0 = time.monotonic()
+    while time.monotonic() - soak_t0 < args.soak:
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    total_ms, per = time_launches(step, args.steps, stream)
+    t1 = time.monotonic()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    clocks = sampler.summary(soak_t0, t1)
+
+    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(elapsed.item())
+    nbytes = adaln_bytes(ROWS, COLS, FRAMES)
+    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    launch_ms = sum(per) / len(per)
+    achieved = nbytes / (launch_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"rmsnorm_adaln_nvfp4 {ROWS}x{COLS} bf16, {FRAMES} frames x {RPF} tokens, "
+                        "per-channel LogNormal(0,0.5) scales",
+            "rows": ROWS, "cols": COLS, "frames": FRAMES, "rows_per_frame": RPF,
+            "l2": f"inputs larger than L2 ({2 * ROWS * COLS / 1e6:.0f} MB bf16 read per step); no flush",
+            "algorithmic_bytes_per_step": nbytes,
+            "rows_per_s": round(world * ROWS * args.steps / (total_ms * 1e-3)),
+            "global_scale": gsf_val,
+            "soak_s": args.soak,
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic("adaln_kernel"),
+            "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                           if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "kernel": "adaln_kernel<14>",
+            "launch_ms": round(launch_ms, 5),
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and not args.no_extras:
+        result["producers"] = measure_producers(h3q, dev, stream, args)
+        result["e2e"] = measure_e2e(h3q, dev, stream, w, gsf, args)
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    elif world > 1:
+        result["e2e"] = measure_e2e(h3q, dev, stream, w, gsf, args, world=world)
+    return result
+
+
+def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
+    """The same metric through the public call with host buffers: each step copies
+    the inputs from pinned host memory, runs the producer, copies codes and scales
+    back to pinned host memory; timed with CUDA events on the stream."""
+    hx = w["x"].cpu().pin_memory()
+    hg = w["gamma"].cpu().pin_memory()
+    ht = w["table"].cpu().pin_memory()
+    hc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8).pin_memory()
+    hs = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8).pin_memory()
+    dx, dg, dt = torch.empty_like(w["x"]), torch.empty_like(w["gamma"]), torch.empty_like(w["table"])
+    dc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    ds = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        dt.copy_(ht, non_blocking=True)
+        h3q.h3q_rmsnorm_adaln_nvfp4(dx, dg, dt, gsf, rows_per_frame=RPF, eps=w["eps"], codes=dc,
+                                    scales=ds, stream=stream)
+        hc.copy_(dc, non_blocking=True)
+        hs.copy_(ds, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 10))
+    total_ms, _ = time_launches(step, steps, stream)
+    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(elapsed.item())
+    nbytes = adaln_bytes(ROWS, COLS, FRAMES)
+    return {
+        "value": round(world * nbytes * steps / (total_ms * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "h2d_bytes_per_step": hx.numel() * 2 + hg.numel() * 2 + ht.numel() * 2,
+        "d2h_bytes_per_step": hc.numel() + hs.numel(),
+        "steps": steps,
+        "ms_per_step": round(total_ms / steps, 3),
+    }
+
+
+def measure_producers(h3q, dev, stream, args):
+    """The other producers, each timed per launch with CUDA events."""
+    peak, _ = hbm_peak()
+    res = {}
+    n = max(5, min(args.steps, 50))
+
+    def entry(nbytes, per, rows):
+        ms = sorted(per)[len(per) // 2]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                "median_launch_ms": round(ms, 5), "rows_per_s": round(rows / (ms * 1e-3)),
+                "algorithmic_bytes": nbytes, "launches": len(per)}
+
+    # SwiGLU 65,280 x 18,944 (5.6 GB per call: larger than L2)
+    gate, up = workloads.swiglu_inputs(dev)
+    g = torch.tensor([calibrate_swiglu_gsf(gate, up)], dtype=torch.float32, device=dev)
+    c, s = h3q.h3q_swiglu_nvfp4(gate, up, g, stream=stream)
+    for _ in range(3):
+        h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)
+    _, per = time_launches(lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream), n, stream)
+    res["swiglu_65280x18944"] = entry(swiglu_bytes(*gate.shape), per, gate.shape[0])
+    del gate, up, c, s
+
+    # attention-output quantize: 65,280 and 300,000 tokens of 56 x 128
+    for tokens in (65280, 300000):
+        x = workloads.attention_output(dev, tokens=tokens)
+        g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
+        c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
+        for _ in range(3):
+            h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream)
+        _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream)
+        res[f"attn_out_quantize_{tokens}x7168"] = entry(quantize_bytes(*x.shape), per, tokens)
+        del x, c, s
+
+    # standalone quantize 8,192 x 7,168 (150 MB: near L2, so L2 is flushed before each launch)
+    x = workloads.quantize_inputs(dev)
+    g = torch.tensor([2688.0 / float(x.float().abs().max())], dtype=torch.float32, device=dev)
+    c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
+    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream,
+                           flush=lambda: scrub.fill_(1))
+    res["quantize_8192x7168_l2_flushed"] = entry(quantize_bytes(*x.shape), per, 8192)
+    del x, c, s, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (cpu_baseline and --impl reference)                                #
+# --------------------------------------------------------------------------- #
+
+def _oracle_adaln_sample(rows: int, seed: int):
+    import numpy as np
+
+    w = workloads.adaln_inputs("cpu", rows=rows, seed=seed)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    frames = (np.arange(rows) + seed * rows) // RPF % FRAMES
+    return bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"]
+
+
+def cpu_baseline(seconds: float = 15.0, rows_per_chunk: int = 255):
+    """The oracle as it stands on the host cores, over chunks of the AdaLN workload
+    until about `seconds` of work has run; GB/s from the same algorithmic bytes."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    oracle.lib()
+    done_rows, spent, chunk = 0, 0.0, 0
+    while spent < seconds:
+        x, gm, tb, fr, eps = _oracle_adaln_sample(rows_per_chunk, seed=100 + chunk)
+        t0 = time.perf_counter()
+        oracle.adaln_rows(x, gm, tb, fr, eps, 1.0, threads=threads)
+        spent += time.perf_counter() - t0
+        done_rows += rows_per_chunk
+        chunk += 1
+    nbytes = done_rows / ROWS * adaln_bytes(ROWS, COLS, FRAMES)
+    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{done_rows} rows x {COLS} of the AdaLN workload ({chunk} chunks of "
+                      f"{rows_per_chunk} rows, {spent:.1f} s on {threads} threads); GB/s by the "
+                      "same algorithmic-byte count as the GPU line"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed on the host cores: each step is a bounded sample of the
+    AdaLN workload (rows_per_step rows), after `warmup` untimed steps."""
+    import oracle
+
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    oracle.lib()
+    rows_per_step = args.reference_rows
+    spent = 0.0
+    for i in range(args.warmup + args.steps):
+        x, gm, tb, fr, eps = _oracle_adaln_sample(rows_per_step, seed=200 + i)
+        t0 = time.perf_counter()
+        oracle.adaln_rows(x, gm, tb, fr, eps, 1.0, threads=threads)
+        if i >= args.warmup:
+            spent += time.perf_counter() - t0
+    nbytes = rows_per_step / ROWS * adaln_bytes(ROWS, COLS, FRAMES) * args.steps
+    value = round(nbytes / spent / 1e9, 4)
+    sample = (f"{rows_per_step} rows x {COLS} of the AdaLN workload per step, {threads} threads; "
+              "GB/s by the same algorithmic-byte count as the GPU line")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"rmsnorm_adaln_nvfp4 {ROWS}x{COLS} bf16 (bounded row sample)",
+                   "rows_per_step": rows_per_step, "cols": COLS},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# --------------------------------------------------------------------------- #
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--reference-rows", type=int, default=510)
+    p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    try:
+        res = run_ours(args, rank, world, dev)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

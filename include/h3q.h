@@ -1,0 +1,175 @@
+/*
+ * h3q.h -- C ABI of the fused NVFP4 activation producers (GB300, sm_103a).
+ *
+ * Three producers turn bf16 activations into NVFP4 GEMM inputs with the
+ * quantize fused into the kernel that produces them, plus a dequantize used
+ * for checking.  Every producer writes:
+ *
+ *   codes   uint8 [rows, cols/2]: E2M1 codes, two per byte, the even column in
+ *           the low nibble (FastVideo compare "fasth3-spark-exact-perf",
+ *           minimax_h3_swiglu_quant.cuh, fp4_pair).  Row pitch cols/2 bytes.
+ *   scales  uint8 [h3q_padded_rows(rows), cols/16]: one E4M3 block scale per
+ *           16 elements, in the 128x4 swizzled layout; the byte of (row r,
+ *           scale column g) is at
+ *             ((r/128)*(cols/64) + g/4)*512 + (r%32)*16 + ((r/32)%4)*4 + g%4.
+ *           Padding rows rows..h3q_padded_rows(rows)-1 are written as zero.
+ *           (FastVideo API page fastvideo.models.vaes.minimax_h3_nvfp4_fused:
+ *           introduction -- "E4M3 block scales, layout_128x4 swizzle, zeroed
+ *           padding rows" -- and new_quantized; the index is written out in
+ *           quant_probe of the FastVideo compare page.)
+ *
+ * Block quantize (16 consecutive elements y of one row, global scale gsf):
+ *   sf = E4M3_rn_satfinite(fl(gsf * fl(amax/6))), dec = fl(E4M3value(sf)/gsf),
+ *   inv = dec != 0 ? fl(1/dec) : 0, code_i = E2M1_rn_satfinite(fl(y_i * inv)).
+ * This is quant_probe of the FastVideo compare page with every approximate
+ * reciprocal replaced by a correctly rounded division.
+ *
+ * Common conventions
+ * ------------------
+ * Memory    All pointers are DEVICE pointers into memory owned by the caller.
+ *           The library never allocates, frees or keeps a pointer after a call
+ *           returns.  Buffers must stay alive until the work queued on
+ *           `stream` has finished.
+ * Stream    `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *           default stream).  Every call is asynchronous: it validates its
+ *           arguments on the host, launches one kernel on `stream` and returns.
+ *           No call synchronises.  The device is the calling thread's current
+ *           CUDA device.
+ * Global    `global_scale` points to one fp32 on the device: the static
+ *   scale   per-tensor scale gsf (finite, > 0; not checked, reading it would
+ *           need a synchronisation).  It is read by the kernel, so it may be
+ *           updated on the stream between calls and captured in a graph.
+ * Shapes    rows >= 0 (rows == 0 is a successful no-op); cols > 0, a multiple
+ *           of 64 (four scale columns form one swizzle atom), at most 2^24.
+ *           ld_* is the row stride of an input in ELEMENTS: >= cols and a
+ *           multiple of 16.  Indexing is 64-bit throughout: inputs larger
+ *           than 2^31 elements are supported (FastVideo commit log, branch
+ *           vae-parallel-decode, the int64 program-id fix).
+ * Alignment bf16 inputs and fp32 outputs: 32-byte aligned.  codes, scales:
+ *           16-byte aligned.  row_frame, global_scale, row_rstd: 4-byte.
+ * Aliasing  Outputs must not overlap inputs or each other.
+ * Errors    H3Q_OK (0) on success.  H3Q_ERR_INVALID_ARGUMENT (1): an argument
+ *           broke a rule above; nothing was launched and no output was
+ *           touched.  H3Q_ERR_CUDA (2): the CUDA runtime reported an error
+ *           (no device, launch failure, or a sticky error from earlier work).
+ *           h3q_last_error() returns a message for the calling thread's most
+ *           recent failure.  No call aborts, traps or prints.
+ * Threads   The calls keep no state between calls except a per-device cache
+ *           of launch sizes; they are safe to call from several threads.
+ */
+#ifndef H3Q_H
+#define H3Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H3Q_OK 0
+#define H3Q_ERR_INVALID_ARGUMENT 1
+#define H3Q_ERR_CUDA 2
+
+#define H3Q_ABI_VERSION 1
+
+/* Rows of the scale matrix: rows rounded up to a multiple of 128. */
+static inline int64_t h3q_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
+/* Bytes of the swizzled scale matrix. */
+static inline int64_t h3q_scale_bytes(int64_t rows, int64_t cols)
+{
+    return h3q_padded_rows(rows) * (cols / 16);
+}
+/* Bytes of the packed code matrix. */
+static inline int64_t h3q_code_bytes(int64_t rows, int64_t cols) { return rows * (cols / 2); }
+
+/*
+ * (c) Standalone NVFP4 quantize, e.g. of the attention output viewed as
+ * [tokens, heads*head_dim].  (TensorRT-LLM PR #21483 "Fuse the MiniMax-H3
+ * NVFP4 activation quantize into the AdaLN, SwiGLU and attention-output
+ * producers", commit "...quantize it with a bandwidth-bound kernel";
+ * FastVideo API page, quantize.)
+ *
+ *   x             bf16 [rows, cols], row stride ld_x elements.
+ *   global_scale  device fp32 gsf.
+ *   codes         out, rows*cols/2 bytes.    scales  out, h3q_scale_bytes.
+ */
+int h3q_quantize_nvfp4(const void *x, int64_t ld_x, int64_t rows, int64_t cols,
+                       const float *global_scale, uint8_t *codes, uint8_t *scales,
+                       void *stream);
+
+/*
+ * (a) RMSNorm with fp32 statistics, AdaLN modulation, NVFP4.  (TensorRT-LLM
+ * PR #21483, summary and commit "...SwiGLU producers": the AdaLN RMSNorm +
+ * modulation kernel emits packed E2M1 codes and swizzled E4M3 scales
+ * directly; FastVideo API page, introduction: fp32 statistics, sequential
+ * FMA per thread, no contraction of products that eager rounds.)
+ *
+ * Per row r with frame t:
+ *   ss   = sum of x^2 in the canonical order: 16-element block b goes to lane
+ *          b % 32; each lane keeps 8 fp32 partials, element e of its blocks
+ *          (blocks in increasing order) is fused-multiply-added into partial
+ *          e % 8; lane total ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)); the 32 lane
+ *          totals are combined by a butterfly over xor-distances 16,8,4,2,1.
+ *   rstd = fl(1 / fl(sqrt(fl(fl(ss / cols) + eps))))
+ *   y    = bf16(fl(fl(fl(fl(x * rstd) * gamma) * fl(1 + scale[t])) + shift[t]))
+ * then y is block-quantized.
+ *
+ *   x               bf16 [rows, cols], row stride ld_x elements.
+ *   gamma           bf16 [cols].
+ *   mod_table       bf16 [num_frames, 2, cols], contiguous: [t][0] is the shift,
+ *                   [t][1] the scale.
+ *   row_frame       int32 [rows] frame of each row, or NULL.  Entries must lie in
+ *                   [0, num_frames) (the index contract of the FastVideo commit
+ *                   log's modulation wrappers).  They are not checked on the
+ *                   host (that would need a synchronisation); the kernel clamps
+ *                   them into range so memory stays safe, and the output of a
+ *                   row with an out-of-range entry is unspecified.
+ *   rows_per_frame  used when row_frame is NULL: frame = row / rows_per_frame;
+ *                   must be >= 1 with (rows-1)/rows_per_frame < num_frames.
+ *   eps             finite, >= 0.
+ *   row_rstd        optional out fp32 [rows]: rstd of each row, or NULL.
+ */
+int h3q_rmsnorm_adaln_nvfp4(const void *x, int64_t ld_x, const void *gamma,
+                            const void *mod_table, int64_t num_frames, const int32_t *row_frame,
+                            int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
+                            const float *global_scale, uint8_t *codes, uint8_t *scales,
+                            float *row_rstd, void *stream);
+
+/*
+ * (b) SwiGLU producer: y = bf16(fl(fl(g * sigma) * u)) with
+ * sigma = fl(1 / fl(1 + exp_c(-g))), then NVFP4.  (FastVideo compare page,
+ * minimax_h3_swiglu_quant.cuh, swiglu_bf16: value * silu(gate) rounded to
+ * bf16; TensorRT-LLM PR #21483, SiLU-and-mul producer.)  exp_c is a fixed
+ * sequence of binary32 operations: Cody-Waite reduction by a two-part ln 2
+ * applied with FMAs and a degree-7 Taylor polynomial in Horner form.
+ *
+ *   gate, up  bf16 [rows, cols], row strides ld_gate, ld_up elements (a
+ *             gate/up pair packed in one [rows, 2*cols] projection is two views
+ *             with ld = 2*cols).
+ */
+int h3q_swiglu_nvfp4(const void *gate, int64_t ld_gate, const void *up, int64_t ld_up,
+                     int64_t rows, int64_t cols, const float *global_scale, uint8_t *codes,
+                     uint8_t *scales, void *stream);
+
+/*
+ * Dequantize (checking path): out[r][j] = fl((E2M1value(c) * E4M3value(sf)) / gsf),
+ * the value a block-scaled NVFP4 GEMM with alpha = 1/gsf sees for the element.
+ * No page defines it; it is the inverse the producers' consumers apply.
+ *
+ *   codes, scales  as written by the producers (scales in the swizzled layout).
+ *   out            fp32 [rows, cols], contiguous.
+ */
+int h3q_dequantize_nvfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t cols,
+                         const float *global_scale, float *out, void *stream);
+
+/* Message for the calling thread's most recent failed call ("" if none). */
+const char *h3q_last_error(void);
+
+/* H3Q_ABI_VERSION of the loaded library. */
+int h3q_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3Q_H */

@@ -1,0 +1,253 @@
+"""h3q -- fused NVFP4 activation producers for GB300 (sm_103a).
+
+A thin Python binding of the C ABI in ``include/h3q.h`` (``libh3q.so``, built
+in-tree by :func:`nvfp4_activation_quantize_gb300.build.build`).  The functions
+carry the C names and only marshal torch CUDA tensors into the C calls; every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+fallback: if the library is missing or no GPU is present the calls raise.
+
+Outputs that are not passed in are allocated here with ``torch.empty`` in the
+shapes of the ABI (codes ``[rows, cols/2]`` uint8, scales
+``[pad128(rows), cols/16]`` uint8 in the 128x4 swizzled layout).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "H3Q_OK", "H3Q_ERR_INVALID_ARGUMENT", "H3Q_ERR_CUDA", "H3QError", "library", "library_path",
+    "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
+    "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
+]
+
+H3Q_OK = 0
+H3Q_ERR_INVALID_ARGUMENT = 1
+H3Q_ERR_CUDA = 2
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SIGNATURES = {
+    "h3q_quantize_nvfp4": [_P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "h3q_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _I64, _I64,
+                                _P, _P, _P, _P, _P],
+    "h3q_swiglu_nvfp4": [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "h3q_dequantize_nvfp4": [_P, _P, _I64, _I64, _P, _P, _P],
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class H3QError(RuntimeError):
+    """A nonzero status from the library, with its message."""
+
+    def __init__(self, fn: str, code: int, message: str):
+        super().__init__(f"{fn} returned {code}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library():
+    """The loaded ``libh3q.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with nvfp4_activation_quantize_gb300.build.build() "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(path)
+            for name, args in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            lib.h3q_last_error.argtypes = []
+            lib.h3q_last_error.restype = ctypes.c_char_p
+            lib.h3q_abi_version.argtypes = []
+            lib.h3q_abi_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def h3q_last_error() -> str:
+    return library().h3q_last_error().decode()
+
+
+def h3q_abi_version() -> int:
+    return library().h3q_abi_version()
+
+
+def padded_rows(rows: int) -> int:
+    return (rows + 127) // 128 * 128
+
+
+def scale_bytes(rows: int, cols: int) -> int:
+    return padded_rows(rows) * (cols // 16)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != H3Q_OK:
+        raise H3QError(fn, rc, h3q_last_error())
+
+
+def _cuda_tensor(name, t, dtype, device=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library takes device pointers)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _rows_view(name, t, dtype, device=None):
+    """A 2-D view with unit column stride; returns (tensor, rows, cols, ld)."""
+    _cuda_tensor(name, t, dtype, device)
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
+    ld = t.stride(0) if t.shape[0] > 1 else t.shape[1]
+    return t, t.shape[0], t.shape[1], ld
+
+
+def _contiguous(name, t, dtype, shape, device):
+    _cuda_tensor(name, t, dtype, device)
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous with shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _outputs(device, rows, cols, codes, scales):
+    import torch
+
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    if scales is None:
+        scales = torch.empty((padded_rows(rows), cols // 16), dtype=torch.uint8, device=device)
+    _contiguous("codes", codes, torch.uint8, (rows, cols // 2), device)
+    _contiguous("scales", scales, torch.uint8, (padded_rows(rows), cols // 16), device)
+    return codes, scales
+
+
+def _gsf(global_scale, device):
+    import torch
+
+    _cuda_tensor("global_scale", global_scale, torch.float32, device)
+    if global_scale.numel() != 1:
+        raise ValueError("global_scale must hold one fp32 value")
+    return global_scale
+
+
+def _stream(stream, device) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def h3q_quantize_nvfp4(x, global_scale, codes=None, scales=None, stream=None):
+    """(c) Standalone NVFP4 quantize of bf16 x [rows, cols]; returns (codes, scales)."""
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    dev = x.device
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_quantize_nvfp4(x.data_ptr(), ld, rows, cols, gsf.data_ptr(),
+                                          codes.data_ptr(), scales.data_ptr(), _stream(stream, dev))
+    _check("h3q_quantize_nvfp4", rc)
+    return codes, scales
+
+
+def h3q_rmsnorm_adaln_nvfp4(x, gamma, mod_table, global_scale, *, row_frame=None,
+                            rows_per_frame=None, eps=1e-6, codes=None, scales=None, row_rstd=None,
+                            stream=None):
+    """(a) RMSNorm (fp32 statistics) + AdaLN modulation + NVFP4 of bf16 x [rows, cols].
+
+    ``mod_table`` is bf16 [frames, 2, cols] ([t, 0] shift, [t, 1] scale); the frame
+    of a row is ``row_frame[row]`` (int32 CUDA tensor) or ``row // rows_per_frame``.
+    ``row_rstd`` (fp32 [rows], optional) receives each row's rstd.
+    Returns (codes, scales).
+    """
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    dev = x.device
+    _contiguous("gamma", gamma, torch.bfloat16, (cols,), dev)
+    _cuda_tensor("mod_table", mod_table, torch.bfloat16, dev)
+    if mod_table.dim() != 3 or mod_table.shape[1:] != (2, cols) or not mod_table.is_contiguous():
+        raise ValueError("mod_table must be contiguous [frames, 2, cols]")
+    frames = mod_table.shape[0]
+    rf_ptr = None
+    if row_frame is not None:
+        _contiguous("row_frame", row_frame, torch.int32, (rows,), dev)
+        rf_ptr = row_frame.data_ptr()
+        rows_per_frame = 0
+    elif rows_per_frame is None:
+        raise ValueError("give row_frame or rows_per_frame")
+    rstd_ptr = None
+    if row_rstd is not None:
+        _contiguous("row_rstd", row_rstd, torch.float32, (rows,), dev)
+        rstd_ptr = row_rstd.data_ptr()
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_rmsnorm_adaln_nvfp4(
+            x.data_ptr(), ld, gamma.data_ptr(), mod_table.data_ptr(), frames, rf_ptr,
+            int(rows_per_frame), float(eps), rows, cols, gsf.data_ptr(), codes.data_ptr(),
+            scales.data_ptr(), rstd_ptr, _stream(stream, dev))
+    _check("h3q_rmsnorm_adaln_nvfp4", rc)
+    return codes, scales
+
+
+def h3q_swiglu_nvfp4(gate, up, global_scale, codes=None, scales=None, stream=None):
+    """(b) NVFP4 of bf16(silu(gate) * up) for bf16 gate, up [rows, cols]; returns (codes, scales)."""
+    import torch
+
+    gate, rows, cols, ldg = _rows_view("gate", gate, torch.bfloat16)
+    dev = gate.device
+    up, rows_u, cols_u, ldu = _rows_view("up", up, torch.bfloat16, dev)
+    if (rows_u, cols_u) != (rows, cols):
+        raise ValueError("gate and up must have the same shape")
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_swiglu_nvfp4(gate.data_ptr(), ldg, up.data_ptr(), ldu, rows, cols,
+                                        gsf.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                                        _stream(stream, dev))
+    _check("h3q_swiglu_nvfp4", rc)
+    return codes, scales
+
+
+def h3q_dequantize_nvfp4(codes, scales, global_scale, out=None, stream=None):
+    """fp32 [rows, cols] = E2M1(code) * E4M3(scale) / gsf (checking path)."""
+    import torch
+
+    _cuda_tensor("codes", codes, torch.uint8)
+    dev = codes.device
+    if codes.dim() != 2 or not codes.is_contiguous():
+        raise ValueError("codes must be contiguous [rows, cols/2]")
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    _contiguous("scales", scales, torch.uint8, (padded_rows(rows), cols // 16), dev)
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    _contiguous("out", out, torch.float32, (rows, cols), dev)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_dequantize_nvfp4(codes.data_ptr(), scales.data_ptr(), rows, cols,
+                                            gsf.data_ptr(), out.data_ptr(), _stream(stream, dev))
+    _check("h3q_dequantize_nvfp4", rc)
+    return out

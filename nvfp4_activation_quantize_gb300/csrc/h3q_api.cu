@@ -1,0 +1,246 @@
+// h3q_api.cu -- the exported C ABI (include/h3q.h): host-side validation, then
+// one kernel launch on the caller's stream.  No allocation, no synchronisation.
+// An argument that breaks the contract returns H3Q_ERR_INVALID_ARGUMENT before
+// any CUDA call, so these checks also run on machines without a GPU.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/h3q.h"
+#include "h3q_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int invalid(const char* fn, const char* what) {
+  return fail(H3Q_ERR_INVALID_ARGUMENT, "%s: %s", fn, what);
+}
+
+int cuda_failed(const char* fn, cudaError_t err) {
+  return fail(H3Q_ERR_CUDA, "%s: CUDA error %d (%s): %s", fn, static_cast<int>(err),
+              cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kMaxCols = int64_t(1) << 24;
+constexpr int64_t kMaxRows = int64_t(1) << 40;
+
+// Byte range [p, p + n) of a buffer, for overlap checks.
+struct Span {
+  uintptr_t lo, hi;
+};
+Span span(const void* p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Bytes spanned by a bf16 [rows, cols] view with row stride ld.
+int64_t view_bytes(int64_t rows, int64_t cols, int64_t ld) { return ((rows - 1) * ld + cols) * 2; }
+
+// Shared shape checks; returns 0 or an error code (message already set).
+int check_shape(const char* fn, int64_t rows, int64_t cols) {
+  if (rows < 0) return invalid(fn, "rows must be >= 0");
+  if (rows > kMaxRows) return invalid(fn, "rows exceeds 2^40");
+  if (cols <= 0 || cols % 64 != 0) return invalid(fn, "cols must be a positive multiple of 64");
+  if (cols > kMaxCols) return invalid(fn, "cols exceeds 2^24");
+  return 0;
+}
+
+int check_input(const char* fn, const char* name, const void* p, int64_t ld, int64_t rows,
+                int64_t cols) {
+  char msg[160];
+  if (p == nullptr) return snprintf(msg, sizeof msg, "%s is NULL", name), invalid(fn, msg);
+  if (!aligned(p, 32)) return snprintf(msg, sizeof msg, "%s must be 32-byte aligned", name), invalid(fn, msg);
+  if (ld < cols || ld % 16 != 0)
+    return snprintf(msg, sizeof msg, "ld of %s must be >= cols and a multiple of 16", name), invalid(fn, msg);
+  if (ld > (int64_t(1) << 62) / (rows > 0 ? rows : 1))
+    return snprintf(msg, sizeof msg, "%s: rows * ld overflows", name), invalid(fn, msg);
+  return 0;
+}
+
+int check_outputs(const char* fn, const uint8_t* codes, const uint8_t* scales,
+                  const float* gsf) {
+  if (codes == nullptr || scales == nullptr) return invalid(fn, "codes and scales must not be NULL");
+  if (!aligned(codes, 16) || !aligned(scales, 16))
+    return invalid(fn, "codes and scales must be 16-byte aligned");
+  if (gsf == nullptr || !aligned(gsf, 4)) return invalid(fn, "global_scale must be a 4-byte aligned pointer");
+  return 0;
+}
+
+// --- per-device, per-kernel launch-size cache -------------------------------
+
+struct OccupancyEntry {
+  const void* kernel;
+  int device;
+  int threads;
+  int blocks_per_sm;
+  int sms;
+};
+std::mutex g_occ_mutex;
+OccupancyEntry g_occ[64];
+int g_occ_n = 0;
+
+}  // namespace
+
+namespace h3q {
+
+cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_blocks, int* blocks) {
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0, sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (int i = 0; i < g_occ_n; ++i)
+      if (g_occ[i].kernel == kernel && g_occ[i].device == device && g_occ[i].threads == threads) {
+        per_sm = g_occ[i].blocks_per_sm;
+        sms = g_occ[i].sms;
+      }
+  }
+  if (per_sm == 0) {
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    if (g_occ_n < 64) g_occ[g_occ_n++] = {kernel, device, threads, per_sm, sms};
+  }
+  int64_t n = static_cast<int64_t>(per_sm) * sms;
+  if (max_blocks < n) n = max_blocks;
+  *blocks = static_cast<int>(n < 1 ? 1 : n);
+  return cudaSuccess;
+}
+
+}  // namespace h3q
+
+extern "C" {
+
+const char* h3q_last_error(void) { return g_last_error.c_str(); }
+
+int h3q_abi_version(void) { return H3Q_ABI_VERSION; }
+
+int h3q_quantize_nvfp4(const void* x, int64_t ld_x, int64_t rows, int64_t cols,
+                       const float* global_scale, uint8_t* codes, uint8_t* scales,
+                       void* stream) {
+  static const char* fn = "h3q_quantize_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  const Span in = span(x, view_bytes(rows, cols, ld_x));
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span s = span(scales, h3q_scale_bytes(rows, cols));
+  if (overlap(in, c) || overlap(in, s) || overlap(c, s)) return invalid(fn, "outputs overlap an input or each other");
+  cudaError_t err = h3q::launch_quantize(static_cast<const uint16_t*>(x), ld_x, rows, cols,
+                                         global_scale, codes, scales,
+                                         static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_rmsnorm_adaln_nvfp4(const void* x, int64_t ld_x, const void* gamma, const void* mod_table,
+                            int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
+                            float eps, int64_t rows, int64_t cols, const float* global_scale,
+                            uint8_t* codes, uint8_t* scales, float* row_rstd, void* stream) {
+  static const char* fn = "h3q_rmsnorm_adaln_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
+  if (num_frames < 1) return invalid(fn, "num_frames must be >= 1");
+  if (num_frames > (int64_t(1) << 31)) return invalid(fn, "num_frames exceeds 2^31");
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_input(fn, "gamma", gamma, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "mod_table", mod_table, cols, 2 * num_frames, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  if (row_frame != nullptr) {
+    if (!aligned(row_frame, 4)) return invalid(fn, "row_frame must be 4-byte aligned");
+  } else {
+    if (rows_per_frame < 1) return invalid(fn, "rows_per_frame must be >= 1 when row_frame is NULL");
+    if ((rows - 1) / rows_per_frame >= num_frames)
+      return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
+  }
+  if (row_rstd != nullptr && !aligned(row_rstd, 4)) return invalid(fn, "row_rstd must be 4-byte aligned");
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span s = span(scales, h3q_scale_bytes(rows, cols));
+  const Span ins[4] = {span(x, view_bytes(rows, cols, ld_x)), span(gamma, cols * 2),
+                       span(mod_table, num_frames * 4 * cols),
+                       row_frame ? span(row_frame, rows * 4) : Span{0, 0}};
+  if (overlap(c, s)) return invalid(fn, "codes and scales overlap");
+  for (const Span& in : ins)
+    if (overlap(in, c) || overlap(in, s)) return invalid(fn, "an output overlaps an input");
+  if (row_rstd != nullptr) {
+    const Span r = span(row_rstd, rows * 4);
+    if (overlap(r, c) || overlap(r, s)) return invalid(fn, "row_rstd overlaps an output");
+    for (const Span& in : ins)
+      if (overlap(in, r)) return invalid(fn, "row_rstd overlaps an input");
+  }
+  cudaError_t err = h3q::launch_adaln(
+      static_cast<const uint16_t*>(x), ld_x, static_cast<const uint16_t*>(gamma),
+      static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, eps, rows,
+      cols, global_scale, codes, scales, row_rstd, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_swiglu_nvfp4(const void* gate, int64_t ld_gate, const void* up, int64_t ld_up,
+                     int64_t rows, int64_t cols, const float* global_scale, uint8_t* codes,
+                     uint8_t* scales, void* stream) {
+  static const char* fn = "h3q_swiglu_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "gate", gate, ld_gate, rows, cols)) return e;
+  if (int e = check_input(fn, "up", up, ld_up, rows, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  const Span g = span(gate, view_bytes(rows, cols, ld_gate));
+  const Span u = span(up, view_bytes(rows, cols, ld_up));
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span s = span(scales, h3q_scale_bytes(rows, cols));
+  if (overlap(g, c) || overlap(g, s) || overlap(u, c) || overlap(u, s) || overlap(c, s))
+    return invalid(fn, "outputs overlap an input or each other");
+  cudaError_t err = h3q::launch_swiglu(static_cast<const uint16_t*>(gate), ld_gate,
+                                       static_cast<const uint16_t*>(up), ld_up, rows, cols,
+                                       global_scale, codes, scales,
+                                       static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                         const float* global_scale, float* out, void* stream) {
+  static const char* fn = "h3q_dequantize_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (codes == nullptr || scales == nullptr || out == nullptr)
+    return invalid(fn, "codes, scales and out must not be NULL");
+  if (!aligned(codes, 16) || !aligned(scales, 16)) return invalid(fn, "codes and scales must be 16-byte aligned");
+  if (!aligned(out, 32)) return invalid(fn, "out must be 32-byte aligned");
+  if (global_scale == nullptr || !aligned(global_scale, 4))
+    return invalid(fn, "global_scale must be a 4-byte aligned pointer");
+  const Span o = span(out, rows * cols * 4);
+  if (overlap(o, span(codes, h3q_code_bytes(rows, cols))) ||
+      overlap(o, span(scales, h3q_scale_bytes(rows, cols))))
+    return invalid(fn, "out overlaps an input");
+  cudaError_t err = h3q::launch_dequantize(codes, scales, rows, cols, global_scale, out,
+                                           static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+}  // extern "C"

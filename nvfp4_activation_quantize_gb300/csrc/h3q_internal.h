@@ -1,0 +1,30 @@
+// h3q_internal.h -- launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace h3q {
+
+// Blocks to launch for a persistent kernel: every SM filled to the occupancy
+// the kernel allows at `threads` threads per block, capped at `max_blocks`.
+// Cached per device and kernel.
+cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_blocks, int* blocks);
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
+                            const float* gsf, uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+
+cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
+                         const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
+                         int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
+                         const float* gsf, uint8_t* codes, uint8_t* scales, float* row_rstd,
+                         cudaStream_t stream);
+
+cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
+                          int64_t ld_up, int64_t rows, int64_t cols, const float* gsf,
+                          uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
+                              int64_t cols, const float* gsf, float* out, cudaStream_t stream);
+
+}  // namespace h3q

@@ -1,0 +1,173 @@
+// swiglu.cu -- (b) SwiGLU producer: y = silu(gate) * up rounded to bf16, then NVFP4.
+//
+// (FastVideo compare "fasth3-spark-exact-perf", minimax_h3_swiglu_quant.cuh,
+// swiglu_bf16: value * silu(gate), one bf16 rounding; TensorRT-LLM PR #21483,
+// the SiLU-and-mul producer that writes NVFP4 directly.)
+//
+// Per element, in binary32 with one rounding per operation:
+//   E = exp_c(-g), sigma = fl(1 / fl(1 + E)), s = fl(g * sigma), y = bf16(fl(s * u))
+// exp_c is this library's fixed exponential: Cody-Waite additive reduction
+// (W. J. Cody and W. Waite, "Software Manual for the Elementary Functions",
+// 1980) by a two-part ln 2 applied with FMAs, and the degree-7 Taylor
+// polynomial of e^r in Horner form:
+//   z > 89 -> +inf, z < -104 -> +0, otherwise
+//   t = fl(z * L2E), k = rint(t), r = fma(-k, C1, z), r = fma(-k, C2, r),
+//   p = P7, p = fma(p, r, Pn) for n = 6..2, p = fma(p, r, 1), p = fma(p, r, 1),
+//   result = p * 2^k rounded once (p * 2^k1 exact, then * 2^(k - k1)).
+//   L2E = fl(1/ln 2), C1 = fl(ln 2), C2 = fl(ln 2 - C1), Pn = fl(1/n!).
+// rint uses the 1.5 * 2^23 addition: for |t| <= 2^22 the sum lands where the
+// binary32 spacing is 1, so the addition itself rounds t half-to-even, and
+// subtracting the constant again is exact.
+//
+// Work layout as in the standalone quantize: one warp per 512-column segment,
+// one 16-element block per lane, 256-bit loads of gate and up.  When every
+// gate of the warp's segment has |g| <= 87 (all data in practice), 2^k is a
+// normal number for every element and the scaling is a single multiply;
+// otherwise the warp takes the two-multiply scaling, which gives identical
+// results wherever both apply.
+#include "h3q_device.cuh"
+#include "h3q_internal.h"
+
+namespace h3q {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 2;
+
+constexpr float kL2E = 0x1.715476p+0f;    // fl(1 / ln 2)
+constexpr float kC1 = 0x1.62e430p-1f;     // fl(ln 2)
+constexpr float kC2 = -0x1.05c610p-29f;   // fl(ln 2 - C1)
+constexpr float kP2 = 0.5f;               // 1/2!
+constexpr float kP3 = 0x1.555556p-3f;     // fl(1/3!)
+constexpr float kP4 = 0x1.555556p-5f;     // fl(1/4!)
+constexpr float kP5 = 0x1.111112p-7f;     // fl(1/5!)
+constexpr float kP6 = 0x1.6c16c2p-10f;    // fl(1/6!)
+constexpr float kP7 = 0x1.a01a02p-13f;    // fl(1/7!)
+constexpr float kRound = 0x1.8p+23f;      // 1.5 * 2^23
+constexpr float kFastLimit = 87.0f;       // |z| <= 87: k in [-126, 127]
+
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+// exp_c of two arguments.  FAST: caller guarantees |z| <= 87.
+template <bool FAST>
+__device__ __forceinline__ float2 exp_c2(float2 z) {
+  float2 zc = z;
+  if (!FAST) {
+    zc.x = fminf(fmaxf(z.x, -104.0f), 89.0f);
+    zc.y = fminf(fmaxf(z.y, -104.0f), 89.0f);
+  }
+  const float2 t = __fmul2_rn(zc, splat(kL2E));
+  const float2 m = __fadd2_rn(t, splat(kRound));
+  const float2 k = __fadd2_rn(m, splat(-kRound));
+  const float2 nk = make_float2(-k.x, -k.y);
+  float2 r = __ffma2_rn(nk, splat(kC1), zc);
+  r = __ffma2_rn(nk, splat(kC2), r);
+  float2 p = splat(kP7);
+  p = __ffma2_rn(p, r, splat(kP6));
+  p = __ffma2_rn(p, r, splat(kP5));
+  p = __ffma2_rn(p, r, splat(kP4));
+  p = __ffma2_rn(p, r, splat(kP3));
+  p = __ffma2_rn(p, r, splat(kP2));
+  p = __ffma2_rn(p, r, splat(1.0f));
+  p = __ffma2_rn(p, r, splat(1.0f));
+  // integer k from the bits of m (spacing 1 around 1.5 * 2^23)
+  const int kx = __float_as_int(m.x) - __float_as_int(kRound);
+  const int ky = __float_as_int(m.y) - __float_as_int(kRound);
+  if (FAST) {
+    const float2 s = make_float2(__int_as_float((kx + 127) << 23), __int_as_float((ky + 127) << 23));
+    return __fmul2_rn(p, s);
+  }
+  const int kx1 = kx >> 1, ky1 = ky >> 1;
+  const float2 s1 = make_float2(__int_as_float((kx1 + 127) << 23), __int_as_float((ky1 + 127) << 23));
+  const float2 s2 = make_float2(__int_as_float((kx - kx1 + 127) << 23),
+                                __int_as_float((ky - ky1 + 127) << 23));
+  float2 e = __fmul2_rn(__fmul2_rn(p, s1), s2);
+  if (z.x > 89.0f) e.x = __int_as_float(0x7f800000);
+  if (z.y > 89.0f) e.y = __int_as_float(0x7f800000);
+  if (z.x < -104.0f) e.x = 0.0f;
+  if (z.y < -104.0f) e.y = 0.0f;
+  return e;
+}
+
+template <bool FAST>
+__device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u, Block16& y) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 gv = bf16x2_to_float2(g.w[i]);
+    const float2 uv = bf16x2_to_float2(u.w[i]);
+    const float2 e = exp_c2<FAST>(make_float2(-gv.x, -gv.y));
+    const float2 d = __fadd2_rn(splat(1.0f), e);
+    const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    const float2 s = __fmul2_rn(gv, sig);
+    y.w[i] = float2_to_bf16x2(__fmul2_rn(s, uv));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
+              int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
+              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const float gsf = *gsf_ptr;
+  const int lane = threadIdx.x & 31;
+  const int64_t groups = cols >> 4;
+  const int64_t quads = cols >> 6;
+  const int64_t segs = (groups + 31) >> 5;
+  const int64_t total = ((rows + 127) >> 7 << 7) * segs;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+
+  for (int64_t s = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); s < total;
+       s += nwarps * kUnroll) {
+    Block16 gb[kUnroll], ub[kUnroll];
+    int64_t row[kUnroll], grp[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t su = s + u * nwarps;
+      row[u] = su / segs;
+      grp[u] = (su - row[u] * segs) * 32 + lane;
+      if (su < total && row[u] < rows && grp[u] < groups) {
+        load_stream(gate + row[u] * ld_gate + grp[u] * kBlock, gb[u]);
+        load_stream(up + row[u] * ld_up + grp[u] * kBlock, ub[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gb[u].w[i] = ub[u].w[i] = 0;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (s + u * nwarps >= total) break;  // warp-uniform
+      const bool in_row = row[u] < rows;
+      const bool in_cols = grp[u] < groups;
+      Block16 y;
+      const bool fast = block_amax(gb[u]) <= kFastLimit;
+      if (__all_sync(0xffffffffu, fast)) {
+        swiglu_block<true>(gb[u], ub[u], y);
+      } else {
+        swiglu_block<false>(gb[u], ub[u], y);
+      }
+      Quantized q = quantize_block(y, gsf);
+      if (!in_row) q.sf = 0;
+      if (in_row && in_cols)
+        store_codes(codes + row[u] * (cols >> 1) + grp[u] * 8, q.codes_lo, q.codes_hi);
+      store_scale_quad(scales, row[u], grp[u], quads, q.sf, in_cols);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
+                          int64_t ld_up, int64_t rows, int64_t cols, const float* gsf,
+                          uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const int64_t segs = (cols / 16 + 31) / 32;
+  const int64_t work = (rows + 127) / 128 * 128 * segs;
+  int blocks = 0;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel), kThreads,
+                                      (work + kWarps - 1) / kWarps, &blocks);
+  if (err != cudaSuccess) return err;
+  swiglu_kernel<<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf, codes,
+                                                 scales);
+  return cudaGetLastError();
+}
+
+}  // namespace h3q

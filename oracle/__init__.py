@@ -69,6 +69,7 @@ _SIGNATURES = {
     "orc_global_scale": ([_F], _F),
     "orc_scale_offset": ([_I64, _I64, _I64], _I64),
     "orc_padded_rows": ([_I64], _I64),
+    "orc_scale_offsets_rows": ([_P, _I64, _I64, _P], None),
     "orc_swizzle_scales": ([_P, _I64, _I64, _P], None),
     "orc_quantize_rows": ([_P, _I64, _I64, _I64, _F, _P, _P, _P], None),
     "orc_row_rstd": ([_P, _I64, _F], _F),
@@ -214,13 +215,9 @@ def scale_offset(row: int, group: int, cols: int) -> int:
 
 def scale_offsets(rows: np.ndarray, cols: int) -> np.ndarray:
     """[len(rows), cols/16] int64 swizzled offsets of the scales of the given rows."""
-    rows = np.asarray(rows, dtype=np.int64)
-    groups = cols // 16
-    out = np.empty((rows.size, groups), np.int64)
-    f = lib().orc_scale_offset
-    for i, r in enumerate(rows.tolist()):
-        for g in range(groups):
-            out[i, g] = f(r, g, cols)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).ravel()
+    out = np.empty((rows.size, cols // 16), np.int64)
+    lib().orc_scale_offsets_rows(_ptr(rows), rows.size, cols, _ptr(out))
     return out
 
 

@@ -292,6 +292,14 @@ int64_t orc_scale_offset(int64_t row, int64_t group, int64_t cols)
 
 int64_t orc_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
 
+/* Offsets of every scale of the listed rows: out is [n, cols/16]. */
+void orc_scale_offsets_rows(const int64_t *rows, int64_t n, int64_t cols, int64_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t g = 0; g < cols / 16; ++g)
+            out[i * (cols / 16) + g] = orc_scale_offset(rows[i], g, cols);
+}
+
 /* sf_logical is [rows, cols/16]; out is pad128(rows) * cols/16 bytes. */
 void orc_swizzle_scales(const uint8_t *sf_logical, int64_t rows, int64_t cols, uint8_t *out)
 {

@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: libh3q.so builds and loads, exports every function
+include/h3q.h declares, and rejects invalid arguments on the host before any
+CUDA call.  (Compute calls need a GPU; they live in the -m gpu tests.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_activation_quantize_gb300 as h3q
+from nvfp4_activation_quantize_gb300 import build as libbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "h3q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return h3q.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(h3q_\w+)\s*\(", text, flags=re.M)
+    inline = set(re.findall(r"static inline [^(]*?(h3q_\w+)\s*\(", text))
+    return sorted(set(names) - inline)
+
+
+def test_header_declares_the_four_calls():
+    names = _declared_functions()
+    for fn in ("h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4", "h3q_swiglu_nvfp4",
+               "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for fn in _declared_functions():
+        assert hasattr(lib, fn), f"{fn} is declared in h3q.h but not exported"
+    assert lib.h3q_abi_version() == 1
+
+
+def _q(lib, x=0x10000, ld=256, rows=4, cols=256, gsf=0x20000, codes=0x30000, scales=0x40000):
+    return lib.h3q_quantize_nvfp4(x, ld, rows, cols, gsf, codes, scales, None)
+
+
+def test_quantize_rejects_bad_arguments_on_the_host(lib):
+    # none of these pointers is dereferenced: validation fails first
+    assert _q(lib, cols=100) == h3q.H3Q_ERR_INVALID_ARGUMENT
+    assert "multiple of 64" in h3q.h3q_last_error()
+    assert _q(lib, cols=0) == 1
+    assert _q(lib, rows=-1) == 1
+    assert _q(lib, x=None) == 1
+    assert _q(lib, x=0x10010) == 1 and "32-byte" in h3q.h3q_last_error()
+    assert _q(lib, ld=200) == 1
+    assert _q(lib, ld=264) == 1
+    assert _q(lib, codes=None) == 1
+    assert _q(lib, scales=0x40004) == 1
+    assert _q(lib, gsf=None) == 1
+    assert _q(lib, codes=0x10000 + 64) == 1 and "overlap" in h3q.h3q_last_error()
+    assert _q(lib, cols=1 << 25, ld=1 << 25) == 1
+
+
+def test_zero_rows_is_a_noop_without_a_gpu(lib):
+    assert _q(lib, rows=0, x=None, codes=None, scales=None, gsf=None) == h3q.H3Q_OK
+    assert h3q.h3q_last_error() == ""
+
+
+def test_adaln_rejects_bad_arguments_on_the_host(lib):
+    def call(**kw):
+        a = dict(x=0x100000, ld=256, gamma=0x200000, table=0x300000, frames=4, row_frame=None,
+                 rpf=16, eps=1e-6, rows=64, cols=256, gsf=0x400000, codes=0x500000,
+                 scales=0x600000, rstd=None)
+        a.update(kw)
+        return lib.h3q_rmsnorm_adaln_nvfp4(a["x"], a["ld"], a["gamma"], a["table"], a["frames"],
+                                           a["row_frame"], a["rpf"], a["eps"], a["rows"], a["cols"],
+                                           a["gsf"], a["codes"], a["scales"], a["rstd"], None)
+
+    assert call(rpf=0) == 1
+    assert call(rpf=15) == 1 and "modulation table" in h3q.h3q_last_error()
+    assert call(frames=0) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(eps=-1.0) == 1
+    assert call(gamma=None) == 1
+    assert call(table=0x300010) == 1
+    assert call(row_frame=0x700002) == 1
+    assert call(rstd=0x600000 + 8) == 1  # rstd inside the scales buffer
+    assert call(codes=0x300000) == 1     # codes over the table
+
+
+def test_swiglu_and_dequantize_reject_bad_arguments_on_the_host(lib):
+    assert lib.h3q_swiglu_nvfp4(0x100000, 256, None, 256, 8, 256, 0x400000, 0x500000, 0x600000,
+                                None) == 1
+    assert lib.h3q_swiglu_nvfp4(0x100000, 256, 0x200000, 8, 8, 256, 0x400000, 0x500000,
+                                0x600000, None) == 1
+    assert lib.h3q_dequantize_nvfp4(0x100000, 0x200000, 8, 256, 0x300000, 0x400010, None) == 1
+    assert lib.h3q_dequantize_nvfp4(0x100000, 0x200000, 8, 96, 0x300000, 0x400000, None) == 1
+
+
+def test_valid_call_without_a_gpu_reports_a_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _q(lib)
+    assert rc == h3q.H3Q_ERR_CUDA, h3q.h3q_last_error()
+    assert "CUDA error" in h3q.h3q_last_error()
+
+
+def test_python_binding_refuses_host_tensors():
+    import torch
+
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        h3q.h3q_quantize_nvfp4(x, torch.ones(1))
