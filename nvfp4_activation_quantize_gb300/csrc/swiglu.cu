@@ -13,7 +13,7 @@
 //   z > 89 -> +inf, z < -104 -> +0, otherwise
 //   t = fl(z * L2E), k = rint(t), r = fma(-k, C1, z), r = fma(-k, C2, r),
 //   p = P7, p = fma(p, r, Pn) for n = 6..2, p = fma(p, r, 1), p = fma(p, r, 1),
-//   result = p * 2^k rounded once (p * 2^k1 exact, then * 2^(k - k1)).
+//   result = p * 2^k rounded once.
 //   L2E = fl(1/ln 2), C1 = fl(ln 2), C2 = fl(ln 2 - C1), Pn = fl(1/n!).
 // rint uses the 1.5 * 2^23 addition: for |t| <= 2^22 the sum lands where the
 // binary32 spacing is 1, so the addition itself rounds t half-to-even, and
@@ -22,9 +22,9 @@
 // Work layout as in the standalone quantize: one warp per 512-column segment,
 // one 16-element block per lane, 256-bit loads of gate and up.  When every
 // gate of the warp's segment has |g| <= 87 (all data in practice), 2^k is a
-// normal number for every element and the scaling is a single multiply;
-// otherwise the warp takes the two-multiply scaling, which gives identical
-// results wherever both apply.
+// normal number for every element and the scaling is a single multiply by a
+// power of two built from k's bits; otherwise the warp scales with ldexpf,
+// which gives identical results wherever both apply.
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
 
@@ -71,18 +71,17 @@ __device__ __forceinline__ float2 exp_c2(float2 z) {
   p = __ffma2_rn(p, r, splat(kP2));
   p = __ffma2_rn(p, r, splat(1.0f));
   p = __ffma2_rn(p, r, splat(1.0f));
-  // integer k from the bits of m (spacing 1 around 1.5 * 2^23)
-  const int kx = __float_as_int(m.x) - __float_as_int(kRound);
-  const int ky = __float_as_int(m.y) - __float_as_int(kRound);
   if (FAST) {
+    // k in [-126, 127]: 2^k is a normal binary32; its exponent field is k + 127,
+    // and k itself sits in the low bits of m (spacing 1 around 1.5 * 2^23).
+    const int kx = __float_as_int(m.x) - __float_as_int(kRound);
+    const int ky = __float_as_int(m.y) - __float_as_int(kRound);
     const float2 s = make_float2(__int_as_float((kx + 127) << 23), __int_as_float((ky + 127) << 23));
     return __fmul2_rn(p, s);
   }
-  const int kx1 = kx >> 1, ky1 = ky >> 1;
-  const float2 s1 = make_float2(__int_as_float((kx1 + 127) << 23), __int_as_float((ky1 + 127) << 23));
-  const float2 s2 = make_float2(__int_as_float((kx - kx1 + 127) << 23),
-                                __int_as_float((ky - ky1 + 127) << 23));
-  float2 e = __fmul2_rn(__fmul2_rn(p, s1), s2);
+  // k in [-150, 128]: ldexpf scales exactly and rounds once (into the subnormal
+  // range or to infinity), which is fl(p * 2^k).
+  float2 e = make_float2(ldexpf(p.x, __float2int_rn(k.x)), ldexpf(p.y, __float2int_rn(k.y)));
   if (z.x > 89.0f) e.x = __int_as_float(0x7f800000);
   if (z.y > 89.0f) e.y = __int_as_float(0x7f800000);
   if (z.x < -104.0f) e.x = 0.0f;
