@@ -484,6 +484,53 @@ def run_reference(args, rank, world):
 
 
 # --------------------------------------------------------------------------- #
+# one producer alone (profiling captures and sweeps)                            #
+# --------------------------------------------------------------------------- #
+
+def run_single(args, dev):
+    """W warm-up and K timed launches of one producer at --rows rows (cols as in the
+    workloads); prints one JSON line.  Used for ncu captures of a small case."""
+    import nvfp4_activation_quantize_gb300 as h3q
+
+    stream = torch.cuda.current_stream(dev)
+    kind = args.kernel
+    if kind == "adaln":
+        rows = args.rows or ROWS
+        w = workloads.adaln_inputs(dev, rows=rows, frames=max(1, -(-rows // RPF)))
+        g = torch.tensor([calibrate_adaln_gsf(w)], dtype=torch.float32, device=dev)
+        c = torch.empty((rows, COLS // 2), dtype=torch.uint8, device=dev)
+        s = torch.empty((padded(rows), COLS // 16), dtype=torch.uint8, device=dev)
+        fn = lambda: h3q.h3q_rmsnorm_adaln_nvfp4(  # noqa: E731
+            w["x"], w["gamma"], w["table"], g, rows_per_frame=RPF, eps=w["eps"], codes=c, scales=s,
+            stream=stream)
+        nbytes = adaln_bytes(rows, COLS, w["table"].shape[0])
+    elif kind == "swiglu":
+        rows = args.rows or ROWS
+        gate, up = workloads.swiglu_inputs(dev, rows=rows)
+        g = torch.tensor([calibrate_swiglu_gsf(gate, up)], dtype=torch.float32, device=dev)
+        c, s = h3q.h3q_swiglu_nvfp4(gate, up, g, stream=stream)
+        fn = lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)  # noqa: E731
+        nbytes = swiglu_bytes(rows, workloads.FFN)
+    else:
+        rows = args.rows or ROWS
+        x = workloads.attention_output(dev, tokens=rows)
+        g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
+        c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
+        fn = lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream)  # noqa: E731
+        nbytes = quantize_bytes(rows, COLS)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    _, per = time_launches(fn, args.steps, stream)
+    ms = sorted(per)[len(per) // 2]
+    peak, _ = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kind, "rows": rows, "median_launch_ms": round(ms, 5), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "algorithmic_bytes": nbytes,
+            "launches": args.steps, "warmup": args.warmup}
+
+
+# --------------------------------------------------------------------------- #
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -496,6 +543,9 @@ def main(argv=None):
     p.add_argument("--reference-rows", type=int, default=510)
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize"],
+                   help="time one producer alone (for profiling); prints a short JSON line")
+    p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -514,6 +564,9 @@ def main(argv=None):
         raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
+    if args.kernel:
+        print(json.dumps(run_single(args, dev)), flush=True)
+        return 0
     if world > 1:
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         torch.distributed.init_process_group("nccl", device_id=dev)
