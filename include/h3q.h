@@ -105,11 +105,12 @@ int h3q_quantize_nvfp4(const void *x, int64_t ld_x, int64_t rows, int64_t cols,
  * FMA per thread, no contraction of products that eager rounds.)
  *
  * Per row r with frame t:
- *   ss   = sum of x^2 in the canonical order: 16-element block b goes to lane
- *          b % 32; each lane keeps 8 fp32 partials, element e of its blocks
- *          (blocks in increasing order) is fused-multiply-added into partial
- *          e % 8; lane total ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)); the 32 lane
- *          totals are combined by a butterfly over xor-distances 16,8,4,2,1.
+ *   ss   = sum of x^2 in the canonical order: 8-element chunk c goes to lane
+ *          c % 128; each lane keeps 8 fp32 partials, element e of its chunks
+ *          (chunks in increasing order) is fused-multiply-added into partial e;
+ *          lane total ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)); within each group of
+ *          32 lanes a butterfly over xor-distances 16,8,4,2,1 gives the group
+ *          total T_w; ss = (T_0+T_1)+(T_2+T_3).
  *   rstd = fl(1 / fl(sqrt(fl(fl(ss / cols) + eps))))
  *   y    = bf16(fl(fl(fl(fl(x * rstd) * gamma) * fl(1 + scale[t])) + shift[t]))
  * then y is block-quantized.

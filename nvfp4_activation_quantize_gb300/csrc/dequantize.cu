@@ -68,7 +68,7 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream) {
   const int64_t segs = (cols / 16 + 31) / 32;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&dequantize_kernel), kThreads,
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&dequantize_kernel), kThreads, 0,
                                       (rows * segs + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
   dequantize_kernel<<<blocks, kThreads, 0, stream>>>(codes, scales, rows, cols, gsf, out);

@@ -89,6 +89,7 @@ struct OccupancyEntry {
   const void* kernel;
   int device;
   int threads;
+  int smem_bytes;
   int blocks_per_sm;
   int sms;
 };
@@ -100,7 +101,8 @@ int g_occ_n = 0;
 
 namespace h3q {
 
-cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_blocks, int* blocks) {
+cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, int64_t max_blocks,
+                              int* blocks) {
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
@@ -108,7 +110,8 @@ cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_block
   {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     for (int i = 0; i < g_occ_n; ++i)
-      if (g_occ[i].kernel == kernel && g_occ[i].device == device && g_occ[i].threads == threads) {
+      if (g_occ[i].kernel == kernel && g_occ[i].device == device && g_occ[i].threads == threads &&
+          g_occ[i].smem_bytes == smem_bytes) {
         per_sm = g_occ[i].blocks_per_sm;
         sms = g_occ[i].sms;
       }
@@ -116,11 +119,15 @@ cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_block
   if (per_sm == 0) {
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (err != cudaSuccess) return err;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (smem_bytes > 48 * 1024) {
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      if (err != cudaSuccess) return err;
+    }
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem_bytes);
     if (err != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     std::lock_guard<std::mutex> lock(g_occ_mutex);
-    if (g_occ_n < 64) g_occ[g_occ_n++] = {kernel, device, threads, per_sm, sms};
+    if (g_occ_n < 64) g_occ[g_occ_n++] = {kernel, device, threads, smem_bytes, per_sm, sms};
   }
   int64_t n = static_cast<int64_t>(per_sm) * sms;
   if (max_blocks < n) n = max_blocks;

@@ -105,17 +105,62 @@ __device__ __forceinline__ uint32_t e2m1x8(float2 a, float2 b, float2 c, float2 
 // Block quantize
 // ---------------------------------------------------------------------------
 
-// Largest |y| of a block of 16 bf16 values, exact: the magnitude bit patterns
-// of non-NaN bf16 values order like the values.
+// max(|a|, |b|) of each bf16 half (the sign bit of the result is the xor of the
+// operands' signs; callers mask it off).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Largest magnitude held in the two halves of a bf16x2 word, as fp32 (exact).
+__device__ __forceinline__ float halves_amax(uint32_t m) {
+  m = absmax_bf16x2(m, __byte_perm(m, 0, 0x1032));
+  return __uint_as_float((m << 16) & 0x7fff0000u);
+}
+
+// Largest |y| of a block of 16 bf16 values, exact.
 __device__ __forceinline__ float block_amax(const Block16& y) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t a = y.w[i] & 0x7fff7fffu;
-    asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
+  const uint32_t a = absmax_bf16x2(absmax_bf16x2(y.w[0], y.w[1]), absmax_bf16x2(y.w[2], y.w[3]));
+  const uint32_t b = absmax_bf16x2(absmax_bf16x2(y.w[4], y.w[5]), absmax_bf16x2(y.w[6], y.w[7]));
+  return halves_amax(absmax_bf16x2(a, b));
+}
+
+// fl(a / 6) for a bf16 value a >= 0 without a division: q0 = fl(a * fl(1/6)) is
+// corrected once by its exact remainder.  Equal to the correctly rounded
+// quotient for every finite such a (checked over all of them in exact
+// arithmetic); +inf (a bf16 overflow of y) is passed through as inf / 6 = inf.
+__device__ __forceinline__ float amax_over_six(float a) {
+  constexpr float kR6 = 0x1.555556p-3f;  // fl(1/6)
+  const float q0 = __fmul_rn(a, kR6);
+  const float rem = __fmaf_rn(-q0, 6.0f, a);
+  const float t = __fmaf_rn(rem, kR6, q0);
+  return a == __int_as_float(0x7f800000) ? a : t;
+}
+
+// Inverse block scale for each E4M3 code under the global scale gsf:
+// inv[sf] = dec != 0 ? fl(1 / dec) : 0 with dec = fl(E4M3value(sf) / gsf).
+// 128 entries in shared memory, filled once per CTA by threads 0..127 (code
+// 0x7F never occurs: the encode saturates at 0x7E).  Call before a barrier.
+__device__ __forceinline__ void fill_inverse_scales(float* inv, float gsf) {
+  const int t = threadIdx.x;
+  if (t < 128) {
+    const float dec = t < 127 ? __fdiv_rn(e4m3_value(static_cast<uint32_t>(t)), gsf) : 0.0f;
+    inv[t] = dec != 0.0f ? __frcp_rn(dec) : 0.0f;
   }
-  const uint32_t hi = m >> 16, lo = m & 0xffffu;
-  return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
+// E4M3 block scale of a block whose largest magnitude is amax:
+// sf = E4M3(fl(gsf * fl(amax / 6))).
+__device__ __forceinline__ uint32_t block_scale(float amax, float gsf) {
+  return e4m3_encode(__fmul_rn(gsf, amax_over_six(amax)));
+}
+
+// Codes of eight bf16 values (four words) under the inverse scale inv.
+__device__ __forceinline__ uint32_t codes8(const uint32_t* w, float inv) {
+  const float2 inv2 = make_float2(inv, inv);
+  return e2m1x8(__fmul2_rn(bf16x2_to_float2(w[0]), inv2), __fmul2_rn(bf16x2_to_float2(w[1]), inv2),
+                __fmul2_rn(bf16x2_to_float2(w[2]), inv2), __fmul2_rn(bf16x2_to_float2(w[3]), inv2));
 }
 
 struct Quantized {
@@ -125,21 +170,14 @@ struct Quantized {
 };
 
 // NVFP4 of one block of bf16 values y under the global scale gsf:
-//   sf = E4M3(fl(gsf * fl(amax / 6))), dec = fl(E4M3value(sf) / gsf),
-//   inv = dec != 0 ? fl(1 / dec) : 0, code_i = E2M1(fl(y_i * inv)).
-__device__ __forceinline__ Quantized quantize_block(const Block16& y, float gsf) {
-  const float amax = block_amax(y);
-  const float s = __fmul_rn(gsf, __fdiv_rn(amax, 6.0f));
+//   sf = E4M3(fl(gsf * fl(amax / 6))), inv = inv_table[sf], code_i = E2M1(fl(y_i * inv)).
+__device__ __forceinline__ Quantized quantize_block(const Block16& y, float gsf,
+                                                    const float* inv_table) {
   Quantized q;
-  q.sf = e4m3_encode(s);
-  const float dec = __fdiv_rn(e4m3_value(q.sf), gsf);
-  const float inv = dec != 0.0f ? __frcp_rn(dec) : 0.0f;
-  const float2 inv2 = make_float2(inv, inv);
-  float2 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(bf16x2_to_float2(y.w[i]), inv2);
-  q.codes_lo = e2m1x8(v[0], v[1], v[2], v[3]);
-  q.codes_hi = e2m1x8(v[4], v[5], v[6], v[7]);
+  q.sf = block_scale(block_amax(y), gsf);
+  const float inv = inv_table[q.sf];
+  q.codes_lo = codes8(y.w, inv);
+  q.codes_hi = codes8(y.w + 4, inv);
   return q;
 }
 

@@ -7,9 +7,12 @@
 namespace h3q {
 
 // Blocks to launch for a persistent kernel: every SM filled to the occupancy
-// the kernel allows at `threads` threads per block, capped at `max_blocks`.
-// Cached per device and kernel.
-cudaError_t persistent_blocks(const void* kernel, int threads, int64_t max_blocks, int* blocks);
+// the kernel allows at `threads` threads and `smem_bytes` of dynamic shared
+// memory per block, capped at `max_blocks`.  Raises the kernel's dynamic
+// shared memory limit when smem_bytes needs it.  Cached per device, kernel
+// and launch shape.
+cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, int64_t max_blocks,
+                              int* blocks);
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
                             const float* gsf, uint8_t* codes, uint8_t* scales, cudaStream_t stream);

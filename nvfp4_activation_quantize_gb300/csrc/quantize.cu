@@ -8,8 +8,9 @@
 // per lane, one 256-bit load per lane (1 KiB contiguous per warp).  Persistent
 // warps walk the segments in an interleaved order so that neighbouring warps
 // read neighbouring kilobytes, and each warp keeps kUnroll segments' loads in
-// flight before it converts any of them.  Segments of the padding rows
-// (rows..pad128(rows)-1) write zero scale words and read nothing.
+// flight before it converts any of them.  A warp steps its (row, segment)
+// positions incrementally, so no division runs per segment.  Segments of the
+// padding rows (rows..pad128(rows)-1) write zero scale words and read nothing.
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
 
@@ -24,25 +25,38 @@ __global__ void __launch_bounds__(kThreads)
 quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
                 const float* __restrict__ gsf_ptr, uint8_t* __restrict__ codes,
                 uint8_t* __restrict__ scales) {
+  __shared__ float inv_table[128];
   const float gsf = *gsf_ptr;
+  fill_inverse_scales(inv_table, gsf);
+  __syncthreads();
+
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
   const int64_t quads = cols >> 6;
   const int64_t segs = (groups + 31) >> 5;
-  const int64_t total = ((rows + 127) >> 7 << 7) * segs;
+  const int64_t prows = (rows + 127) >> 7 << 7;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
 
-  for (int64_t s = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); s < total;
-       s += nwarps * kUnroll) {
+  // (row, segment) of the kUnroll segments this warp handles per step, and the
+  // advance of one step (nwarps * kUnroll segments) in rows and segments.
+  int64_t row[kUnroll], seg[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t s = first + u * nwarps;
+    row[u] = s / segs;
+    seg[u] = s - row[u] * segs;
+  }
+  const int64_t adv_rows = nwarps * kUnroll / segs;
+  const int64_t adv_segs = nwarps * kUnroll - adv_rows * segs;
+
+  while (row[0] < prows) {
     Block16 in[kUnroll];
-    int64_t row[kUnroll], grp[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t su = s + u * nwarps;
-      row[u] = su / segs;
-      grp[u] = (su - row[u] * segs) * 32 + lane;
-      if (su < total && row[u] < rows && grp[u] < groups) {
-        load_stream(x + row[u] * ld + grp[u] * kBlock, in[u]);
+      const int64_t g = seg[u] * 32 + lane;
+      if (row[u] < rows && g < groups) {
+        load_stream(x + row[u] * ld + g * kBlock, in[u]);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) in[u].w[i] = 0;
@@ -50,14 +64,24 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (s + u * nwarps >= total) break;  // warp-uniform
+      if (row[u] >= prows) break;  // warp-uniform
+      const int64_t g = seg[u] * 32 + lane;
       const bool in_row = row[u] < rows;
-      const bool in_cols = grp[u] < groups;
-      Quantized q = quantize_block(in[u], gsf);
+      const bool in_cols = g < groups;
+      Quantized q = quantize_block(in[u], gsf, inv_table);
       if (!in_row) q.sf = 0;
       if (in_row && in_cols)
-        store_codes(codes + row[u] * (cols >> 1) + grp[u] * 8, q.codes_lo, q.codes_hi);
-      store_scale_quad(scales, row[u], grp[u], quads, q.sf, in_cols);
+        store_codes(codes + row[u] * (cols >> 1) + g * 8, q.codes_lo, q.codes_hi);
+      store_scale_quad(scales, row[u], g, quads, q.sf, in_cols);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      row[u] += adv_rows;
+      seg[u] += adv_segs;
+      if (seg[u] >= segs) {
+        seg[u] -= segs;
+        row[u] += 1;
+      }
     }
   }
 }
@@ -70,7 +94,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t ld, int64_t rows, int64_t
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&quantize_kernel), kThreads,
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&quantize_kernel), kThreads, 0,
                                       (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
   quantize_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, gsf, codes, scales);

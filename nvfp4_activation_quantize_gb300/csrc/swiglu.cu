@@ -49,31 +49,38 @@ constexpr float kFastLimit = 87.0f;       // |z| <= 87: k in [-126, 127]
 
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
-// exp_c of two arguments.  FAST: caller guarantees |z| <= 87.
+// exp_c(-g) for two gates g, with the negation folded away:
+//   t  = fl(-g * L2E)        = fl(g * -L2E)
+//   r1 = fma(-k, C1, -g)     = -fma(k, C1, g)       (so r' = fma(k, C1, g) = -r1)
+//   r2 = fma(-k, C2, r1)     = -fma(k, C2, r')      (so r' = fma(k, C2, r') = -r2)
+// and Horner in r = -r' run as Horner in r' with the coefficient of r^n
+// multiplied by (-1)^n: every intermediate is the exact negation or copy of
+// the one in the r form, because round-to-nearest is odd-symmetric.  The
+// results are the bits exp_c defines.
+// FAST: every |g| <= 87, so k lies in [-126, 127] and 2^k is normal.
 template <bool FAST>
-__device__ __forceinline__ float2 exp_c2(float2 z) {
-  float2 zc = z;
-  if (!FAST) {
-    zc.x = fminf(fmaxf(z.x, -104.0f), 89.0f);
-    zc.y = fminf(fmaxf(z.y, -104.0f), 89.0f);
+__device__ __forceinline__ float2 exp_neg2(float2 g) {
+  float2 gc = g;
+  if (!FAST) {  // z = -g clamped to [-104, 89]
+    gc.x = fminf(fmaxf(g.x, -89.0f), 104.0f);
+    gc.y = fminf(fmaxf(g.y, -89.0f), 104.0f);
   }
-  const float2 t = __fmul2_rn(zc, splat(kL2E));
+  const float2 t = __fmul2_rn(gc, splat(-kL2E));
   const float2 m = __fadd2_rn(t, splat(kRound));
   const float2 k = __fadd2_rn(m, splat(-kRound));
-  const float2 nk = make_float2(-k.x, -k.y);
-  float2 r = __ffma2_rn(nk, splat(kC1), zc);
-  r = __ffma2_rn(nk, splat(kC2), r);
-  float2 p = splat(kP7);
+  float2 r = __ffma2_rn(k, splat(kC1), gc);
+  r = __ffma2_rn(k, splat(kC2), r);
+  float2 p = splat(-kP7);
   p = __ffma2_rn(p, r, splat(kP6));
-  p = __ffma2_rn(p, r, splat(kP5));
+  p = __ffma2_rn(p, r, splat(-kP5));
   p = __ffma2_rn(p, r, splat(kP4));
-  p = __ffma2_rn(p, r, splat(kP3));
+  p = __ffma2_rn(p, r, splat(-kP3));
   p = __ffma2_rn(p, r, splat(kP2));
-  p = __ffma2_rn(p, r, splat(1.0f));
+  p = __ffma2_rn(p, r, splat(-1.0f));
   p = __ffma2_rn(p, r, splat(1.0f));
   if (FAST) {
-    // k in [-126, 127]: 2^k is a normal binary32; its exponent field is k + 127,
-    // and k itself sits in the low bits of m (spacing 1 around 1.5 * 2^23).
+    // 2^k is a normal binary32; its exponent field is k + 127, and k itself sits
+    // in the low bits of m (spacing 1 around 1.5 * 2^23).
     const int kx = __float_as_int(m.x) - __float_as_int(kRound);
     const int ky = __float_as_int(m.y) - __float_as_int(kRound);
     const float2 s = make_float2(__int_as_float((kx + 127) << 23), __int_as_float((ky + 127) << 23));
@@ -82,10 +89,10 @@ __device__ __forceinline__ float2 exp_c2(float2 z) {
   // k in [-150, 128]: ldexpf scales exactly and rounds once (into the subnormal
   // range or to infinity), which is fl(p * 2^k).
   float2 e = make_float2(ldexpf(p.x, __float2int_rn(k.x)), ldexpf(p.y, __float2int_rn(k.y)));
-  if (z.x > 89.0f) e.x = __int_as_float(0x7f800000);
-  if (z.y > 89.0f) e.y = __int_as_float(0x7f800000);
-  if (z.x < -104.0f) e.x = 0.0f;
-  if (z.y < -104.0f) e.y = 0.0f;
+  if (g.x < -89.0f) e.x = __int_as_float(0x7f800000);  // z > 89
+  if (g.y < -89.0f) e.y = __int_as_float(0x7f800000);
+  if (g.x > 104.0f) e.x = 0.0f;                        // z < -104
+  if (g.y > 104.0f) e.y = 0.0f;
   return e;
 }
 
@@ -95,7 +102,7 @@ __device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u,
   for (int i = 0; i < 8; ++i) {
     const float2 gv = bf16x2_to_float2(g.w[i]);
     const float2 uv = bf16x2_to_float2(u.w[i]);
-    const float2 e = exp_c2<FAST>(make_float2(-gv.x, -gv.y));
+    const float2 e = exp_neg2<FAST>(gv);
     const float2 d = __fadd2_rn(splat(1.0f), e);
     const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
     const float2 s = __fmul2_rn(gv, sig);
@@ -107,26 +114,37 @@ __global__ void __launch_bounds__(kThreads)
 swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
               int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  __shared__ float inv_table[128];
   const float gsf = *gsf_ptr;
+  fill_inverse_scales(inv_table, gsf);
+  __syncthreads();
+
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
   const int64_t quads = cols >> 6;
   const int64_t segs = (groups + 31) >> 5;
-  const int64_t total = ((rows + 127) >> 7 << 7) * segs;
+  const int64_t prows = (rows + 127) >> 7 << 7;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
 
-  for (int64_t s = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); s < total;
-       s += nwarps * kUnroll) {
+  int64_t row[kUnroll], seg[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t s = first + u * nwarps;
+    row[u] = s / segs;
+    seg[u] = s - row[u] * segs;
+  }
+  const int64_t adv_rows = nwarps * kUnroll / segs;
+  const int64_t adv_segs = nwarps * kUnroll - adv_rows * segs;
+
+  while (row[0] < prows) {
     Block16 gb[kUnroll], ub[kUnroll];
-    int64_t row[kUnroll], grp[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t su = s + u * nwarps;
-      row[u] = su / segs;
-      grp[u] = (su - row[u] * segs) * 32 + lane;
-      if (su < total && row[u] < rows && grp[u] < groups) {
-        load_stream(gate + row[u] * ld_gate + grp[u] * kBlock, gb[u]);
-        load_stream(up + row[u] * ld_up + grp[u] * kBlock, ub[u]);
+      const int64_t g = seg[u] * 32 + lane;
+      if (row[u] < rows && g < groups) {
+        load_stream(gate + row[u] * ld_gate + g * kBlock, gb[u]);
+        load_stream(up + row[u] * ld_up + g * kBlock, ub[u]);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) gb[u].w[i] = ub[u].w[i] = 0;
@@ -134,9 +152,10 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (s + u * nwarps >= total) break;  // warp-uniform
+      if (row[u] >= prows) break;  // warp-uniform
+      const int64_t g = seg[u] * 32 + lane;
       const bool in_row = row[u] < rows;
-      const bool in_cols = grp[u] < groups;
+      const bool in_cols = g < groups;
       Block16 y;
       const bool fast = block_amax(gb[u]) <= kFastLimit;
       if (__all_sync(0xffffffffu, fast)) {
@@ -144,11 +163,20 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       } else {
         swiglu_block<false>(gb[u], ub[u], y);
       }
-      Quantized q = quantize_block(y, gsf);
+      Quantized q = quantize_block(y, gsf, inv_table);
       if (!in_row) q.sf = 0;
       if (in_row && in_cols)
-        store_codes(codes + row[u] * (cols >> 1) + grp[u] * 8, q.codes_lo, q.codes_hi);
-      store_scale_quad(scales, row[u], grp[u], quads, q.sf, in_cols);
+        store_codes(codes + row[u] * (cols >> 1) + g * 8, q.codes_lo, q.codes_hi);
+      store_scale_quad(scales, row[u], g, quads, q.sf, in_cols);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      row[u] += adv_rows;
+      seg[u] += adv_segs;
+      if (seg[u] >= segs) {
+        seg[u] -= segs;
+        row[u] += 1;
+      }
     }
   }
 }
@@ -161,7 +189,7 @@ cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t*
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel), kThreads,
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel), kThreads, 0,
                                       (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
   swiglu_kernel<<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf, codes,

@@ -338,36 +338,44 @@ void orc_quantize_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t l
 }
 
 /*
- * RMS statistics of one row in the canonical order.  The row's 16-element
- * blocks are dealt round-robin to 32 lanes (block b to lane b % 32).  Each
- * lane keeps eight fp32 partial sums; element e of each of its blocks, in
- * increasing block order and increasing e, goes into partial e % 8 through a
- * fused multiply-add ("sequential FMA per thread", [FV-API] introduction).
- * A lane's total is ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)); the 32 lane totals
- * are then combined by a butterfly: for o = 16, 8, 4, 2, 1 every lane adds
- * the total of lane (l xor o).  Finally
+ * RMS statistics of one row in the canonical order.  The row's 8-element
+ * chunks (chunk c = columns 8c..8c+7) are dealt round-robin to 128 lanes
+ * (chunk c to lane c % 128).  Each lane keeps eight fp32 partials; element e
+ * of each of its chunks, chunks in increasing order, goes into partial e
+ * through a fused multiply-add ("sequential FMA per thread", [FV-API]
+ * introduction).  A lane's total is ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).  The
+ * lanes form four groups of 32 (lanes 32w..32w+31); inside a group a
+ * butterfly -- for o = 16, 8, 4, 2, 1 every lane adds the total of lane
+ * (l xor o) -- leaves each lane holding the group total T_w, and
+ *   ss   = (T_0 + T_1) + (T_2 + T_3)
  *   mean = fl(ss / cols),  rstd = fl(1 / fl(sqrt(fl(mean + eps)))).
  */
 float orc_row_rstd(const uint16_t *xrow, int64_t cols, float eps)
 {
-    int64_t blocks = cols / 16;
-    float lane[32];
-    for (int l = 0; l < 32; ++l) {
+    int64_t chunks = cols / 8;
+    float lane[128];
+    for (int l = 0; l < 128; ++l) {
         float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        for (int64_t b = l; b < blocks; b += 32)
-            for (int e = 0; e < 16; ++e) {
-                float v = orc_bf16_value(xrow[16 * b + e]);
-                p[e % 8] = fmaf(v, v, p[e % 8]);
+        for (int64_t c = l; c < chunks; c += 128)
+            for (int e = 0; e < 8; ++e) {
+                float v = orc_bf16_value(xrow[8 * c + e]);
+                p[e] = fmaf(v, v, p[e]);
             }
         lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
     }
-    for (int o = 16; o >= 1; o /= 2) {
-        float next[32];
-        for (int l = 0; l < 32; ++l)
-            next[l] = lane[l] + lane[l ^ o];
-        memcpy(lane, next, sizeof lane);
+    float group[4];
+    for (int w = 0; w < 4; ++w) {
+        float g[32];
+        memcpy(g, lane + 32 * w, sizeof g);
+        for (int o = 16; o >= 1; o /= 2) {
+            float next[32];
+            for (int l = 0; l < 32; ++l)
+                next[l] = g[l] + g[l ^ o];
+            memcpy(g, next, sizeof g);
+        }
+        group[w] = g[0];
     }
-    float ss = lane[0];
+    float ss = (group[0] + group[1]) + (group[2] + group[3]);
     float mean = ss / (float)cols;
     float root = sqrtf(mean + eps);
     return 1.0f / root;
