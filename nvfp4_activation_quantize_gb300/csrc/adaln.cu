@@ -21,10 +21,12 @@
 // thread keeps gamma, 1+scale and shift of its own chunks in registers as fp32
 // and reloads them only when the frame changes.  Neither the modulation table
 // nor gamma is re-read per row.
-// x streams through a ring of kStages rows in shared memory filled with
-// cp.async: each thread copies exactly the chunks it will read, so the data
-// needs no barrier, only the thread's own cp.async.wait_group; kStages-1 rows
-// per CTA are in flight while one is computed.
+// x streams through a ring of kPairStages row pairs in shared memory filled
+// with cp.async: each thread copies exactly the chunks it will read, so the
+// data needs no barrier, only the thread's own cp.async.wait_group; two pairs
+// per CTA are in flight while one is computed.  Rows are processed in pairs,
+// which shares one barrier and the table registers between two independent
+// rows' arithmetic.
 // Rows wider than 8,192 take a generic kernel with the same chunk-to-thread
 // mapping and order that reads x twice and the tables per row.
 #include "h3q_device.cuh"
@@ -34,7 +36,7 @@ namespace h3q {
 namespace {
 
 constexpr int kThreads = 128;  // the lanes of the canonical order
-constexpr int kStages = 4;     // rows of x per CTA in the cp.async ring
+constexpr int kPairStages = 3;  // row pairs of x per CTA in the cp.async ring
 
 struct AdalnArgs {
   const uint16_t* x;
@@ -80,14 +82,42 @@ __device__ __forceinline__ uint4 load16_stream(const uint16_t* p) {
   return v;
 }
 
-__device__ __forceinline__ int64_t frame_of(const AdalnArgs& a, int64_t row) {
-  int64_t t = a.row_frame ? static_cast<int64_t>(a.row_frame[row]) : row / a.rows_per_frame;
+__device__ __forceinline__ int64_t clamp_frame(const AdalnArgs& a, int64_t t) {
   return t < 0 ? 0 : (t >= a.num_frames ? a.num_frames - 1 : t);  // memory safety only
 }
 
-// fp32 gamma, 1 + scale and shift of chunk c of frame t.
-__device__ __forceinline__ void load_tables(const AdalnArgs& a, int64_t t, int64_t c, float* gm,
-                                            float* fc, float* sh) {
+__device__ __forceinline__ int64_t frame_of(const AdalnArgs& a, int64_t row) {
+  return clamp_frame(a, a.row_frame ? static_cast<int64_t>(a.row_frame[row]) : row / a.rows_per_frame);
+}
+
+// Frame of increasing rows without a division per row: with rows_per_frame the
+// cursor keeps the first row of the next frame and steps across boundaries.
+struct FrameCursor {
+  int64_t frame, next;
+  __device__ __forceinline__ FrameCursor(const AdalnArgs& a, int64_t row) {
+    frame = a.row_frame ? 0 : row / a.rows_per_frame;
+    next = a.row_frame ? 0 : (frame + 1) * a.rows_per_frame;
+  }
+  __device__ __forceinline__ int64_t at(const AdalnArgs& a, int64_t row) {
+    if (a.row_frame) return clamp_frame(a, a.row_frame[row]);
+    while (row >= next) {
+      ++frame;
+      next += a.rows_per_frame;
+    }
+    return clamp_frame(a, frame);
+  }
+};
+
+// gamma and 1 + scale of chunk c of frame t as fp32 pairs (elements 2i, 2i+1)
+// for the paired multiplies, and the shift as the bf16 pairs it is stored in
+// (the final add takes bf16 operands directly).
+struct ChunkTables {
+  float2 gm[4], fc[4];
+  uint32_t sh[4];
+};
+
+__device__ __forceinline__ void load_tables(const AdalnArgs& a, int64_t t, int64_t c,
+                                            ChunkTables& tb) {
   const uint16_t* shift = a.table + t * 2 * a.cols + c * 8;
   const uint4 g4 = load16_reused(a.gamma + c * 8);
   const uint4 s4 = load16_reused(shift + a.cols);
@@ -97,12 +127,9 @@ __device__ __forceinline__ void load_tables(const AdalnArgs& a, int64_t t, int64
   const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 g = bf16x2_to_float2(gw[i]);
-    const float2 f = __fadd2_rn(make_float2(1.0f, 1.0f), bf16x2_to_float2(sw[i]));
-    const float2 h = bf16x2_to_float2(hw[i]);
-    gm[2 * i] = g.x, gm[2 * i + 1] = g.y;
-    fc[2 * i] = f.x, fc[2 * i + 1] = f.y;
-    sh[2 * i] = h.x, sh[2 * i + 1] = h.y;
+    tb.gm[i] = bf16x2_to_float2(gw[i]);
+    tb.fc[i] = add2(make_float2(1.0f, 1.0f), bf16x2_to_float2(sw[i]));
+    tb.sh[i] = hw[i];
   }
 }
 
@@ -112,23 +139,48 @@ __device__ __forceinline__ void accumulate(const uint4& v, float2 (&acc)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = bf16x2_to_float2(w[i]);
-    acc[i] = __ffma2_rn(f, f, acc[i]);
+    acc[i] = fma2(f, f, acc[i]);
   }
 }
 
-// ss of the row from this thread's partials: lane total, warp butterfly, then
-// (T0+T1)+(T2+T3) over the four warps.  `slot` alternates between rows so one
-// barrier per row suffices.
-__device__ __forceinline__ float row_sum_of_squares(const float2 (&acc)[4], float (*totals)[4],
-                                                    int slot) {
-  float tot = __fadd_rn(__fadd_rn(__fadd_rn(acc[0].x, acc[0].y), __fadd_rn(acc[1].x, acc[1].y)),
-                        __fadd_rn(__fadd_rn(acc[2].x, acc[2].y), __fadd_rn(acc[3].x, acc[3].y)));
+// Row sums of squares of R rows from this thread's partials, in two halves
+// around a CTA barrier: post_totals forms the lane totals, runs the warp
+// butterfly and leaves each warp's total in totals[slot]; after a barrier,
+// gather_totals combines the four warp totals as (T0+T1)+(T2+T3).
+template <int R>
+__device__ __forceinline__ void post_totals(const float2 (&acc)[R][4], float (*totals)[R][4],
+                                            int slot) {
+  float tot[R];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, o));
-  if ((threadIdx.x & 31) == 0) totals[slot][threadIdx.x >> 5] = tot;
+  for (int k = 0; k < R; ++k) {
+    tot[k] = __fadd_rn(
+        __fadd_rn(__fadd_rn(acc[k][0].x, acc[k][0].y), __fadd_rn(acc[k][1].x, acc[k][1].y)),
+        __fadd_rn(__fadd_rn(acc[k][2].x, acc[k][2].y), __fadd_rn(acc[k][3].x, acc[k][3].y)));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < R; ++k) tot[k] = __fadd_rn(tot[k], __shfl_xor_sync(0xffffffffu, tot[k], o));
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int k = 0; k < R; ++k) totals[slot][k][threadIdx.x >> 5] = tot[k];
+}
+
+template <int R>
+__device__ __forceinline__ void gather_totals(float (*totals)[R][4], int slot, float (&ss)[R]) {
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const float* T = totals[slot][k];
+    ss[k] = __fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3]));
+  }
+}
+
+template <int R>
+__device__ __forceinline__ void row_sums(const float2 (&acc)[R][4], float (*totals)[R][4],
+                                         int slot, float (&ss)[R]) {
+  post_totals<R>(acc, totals, slot);
   __syncthreads();
-  const float* T = totals[slot];
-  return __fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3]));
+  gather_totals<R>(totals, slot, ss);
 }
 
 __device__ __forceinline__ float rstd_of(float ss, int64_t cols, float eps) {
@@ -136,37 +188,61 @@ __device__ __forceinline__ float rstd_of(float ss, int64_t cols, float eps) {
   return __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
 }
 
-// Modulate chunk c (x words v) of row `row`, quantize this thread's half
-// block, store its four code bytes and, from the first lane of each group of
-// eight, the scale word of the four blocks of the group.  All 32 lanes of the
-// warp call this (it shuffles); `valid` masks the stores.
-__device__ __forceinline__ void emit_chunk(const AdalnArgs& a, int64_t row, int64_t c, bool valid,
-                                           const uint4& v, float rstd, const float* gm,
-                                           const float* fc, const float* sh, float gsf,
+// Byte offset of row r's part of a scale word: everything of the swizzled index
+// but the scale-column quad (which adds quad * 512).
+__device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
+  return (r >> 7) * quads * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
+// Modulate one chunk of R rows (x words v[k], statistics rstd[k]) with the
+// chunk's tables, quantize this thread's half block of each row, store its four
+// code bytes at codes_at[k] and, from the first lane of each group of eight,
+// the scale word of the group's four blocks at scale_at[k].  All 32 lanes of
+// the warp call this (it shuffles); `valid` masks the stores.
+template <int R>
+__device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rstd)[R],
+                                           const ChunkTables& tb, bool valid,
+                                           uint8_t* const (&codes_at)[R],
+                                           uint8_t* const (&scale_at)[R], float gsf,
                                            const float* inv_table) {
-  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
-  const float2 rstd2 = make_float2(rstd, rstd);
-  uint32_t y[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 n = __fmul2_rn(bf16x2_to_float2(xw[i]), rstd2);
-    const float2 h = __fmul2_rn(n, make_float2(gm[2 * i], gm[2 * i + 1]));
-    const float2 m = __fmul2_rn(h, make_float2(fc[2 * i], fc[2 * i + 1]));
-    const float2 o = __fadd2_rn(m, make_float2(sh[2 * i], sh[2 * i + 1]));
-    y[i] = float2_to_bf16x2(o);
-  }
   const int lane = threadIdx.x & 31;
-  const float half_amax = halves_amax(absmax_bf16x2(absmax_bf16x2(y[0], y[1]),
-                                                    absmax_bf16x2(y[2], y[3])));
-  const float amax = fmaxf(half_amax, __shfl_xor_sync(0xffffffffu, half_amax, 1));
-  const uint32_t sf = block_scale(amax, gsf);
-  const uint32_t codes = codes8(y, inv_table[sf]);
-  if (valid) store_word(a.codes + row * (a.cols >> 1) + c * 4, codes);
-  uint32_t word = (lane & 1) ? 0u : sf << (8 * ((lane >> 1) & 3));
-  word |= __shfl_xor_sync(0xffffffffu, word, 2);
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
+  // Stages run across all R rows before the next stage, so that the rows'
+  // independent work sits side by side for the scheduler.
+  uint32_t y[R][4];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const uint32_t xw[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+    const float2 rstd2 = make_float2(rstd[k], rstd[k]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 n = mul2(bf16x2_to_float2(xw[i]), rstd2);
+      const float2 h = mul2(n, tb.gm[i]);
+      const float2 m = mul2(h, tb.fc[i]);
+      y[k][i] = float2_to_bf16x2(add_bf16x2_f32(tb.sh[i], m));
+    }
+  }
+  float amax[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k)
+    amax[k] = halves_amax(absmax_bf16x2(absmax_bf16x2(y[k][0], y[k][1]),
+                                        absmax_bf16x2(y[k][2], y[k][3])));
+#pragma unroll
+  for (int k = 0; k < R; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], 1));
+  uint32_t sf[R], word[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    sf[k] = block_scale(amax[k], gsf);
+    const uint32_t codes = codes8(y[k], inv_table[sf[k]]);
+    if (valid) store_word(codes_at[k], codes);
+    word[k] = (lane & 1) ? 0u : sf[k] << (8 * ((lane >> 1) & 3));
+  }
+#pragma unroll
+  for (int k = 0; k < R; ++k) word[k] |= __shfl_xor_sync(0xffffffffu, word[k], 2);
+#pragma unroll
+  for (int k = 0; k < R; ++k) word[k] |= __shfl_xor_sync(0xffffffffu, word[k], 4);
   if (valid && (lane & 7) == 0)
-    store_word(a.scales + scale_word_offset(row, c >> 3, a.cols >> 6), word);
+#pragma unroll
+    for (int k = 0; k < R; ++k) store_word(scale_at[k], word[k]);
 }
 
 // Zero scale words of the padding rows rows..pad128(rows)-1, spread over CTAs.
@@ -179,116 +255,199 @@ __device__ __forceinline__ void zero_padding_rows(const AdalnArgs& a) {
 }
 
 // Rows up to 128 * CPL chunks (CPL * 1,024 columns): tables resident in
-// registers, x through the cp.async ring in dynamic shared memory laid out as
-// [kStages][CPL][128] 16-byte chunks (each warp's 32 chunks are contiguous).
+// registers, x through a cp.async ring in dynamic shared memory laid out as
+// [kPairStages][2][CPL][128] 16-byte chunks (each warp's 32 chunks contiguous).
+// Rows go in consecutive pairs: one barrier per pair, and the two rows'
+// independent arithmetic interleaves under the same table registers.  A pair
+// whose rows lie in different frames is emitted one row at a time.
 template <int CPL>
 __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
   extern __shared__ uint4 ring[];
   __shared__ float inv_table[128];
-  __shared__ float totals[2][4];
+  __shared__ float totals[2][2][4];
   const float gsf = *a.gsf;
   fill_inverse_scales(inv_table, gsf);
 
   const int t = threadIdx.x;
   const int64_t chunks = a.cols >> 3;
+  const int64_t quads = a.cols >> 6;
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
   const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
+  const int64_t pairs = (r_end - r_begin + 1) >> 1;
   const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
-  // Copy this thread's chunks of row r into ring stage s; always commit a
+  // Copy this thread's chunks of pair p into ring stage s; always commit a
   // group (empty past the range) so that group counting stays uniform.
-  auto issue = [&](int64_t r, int s) {
-    if (r < r_end) {
-      const uint16_t* xr = a.x + r * a.ld;
+  const uint16_t* x_t = a.x + t * 8;                      // this thread's first chunk
+  const uint32_t ring_t = ring_base + t * 16;
+  auto issue = [&](int64_t p, int s) {
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int64_t c = t + j * kThreads;
-        if (c < chunks) cp_async16(ring_base + ((s * CPL + j) * kThreads + t) * 16, xr + c * 8);
+    for (int k = 0; k < 2; ++k) {
+      const int64_t r = r_begin + 2 * p + k;
+      if (r < r_end) {
+        const uint16_t* xr = x_t + r * a.ld;
+        const uint32_t dst = ring_t + (s * 2 + k) * (CPL * kThreads * 16);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+          if (t + j * kThreads < chunks) cp_async16(dst + j * (kThreads * 16), xr + j * (kThreads * 8));
       }
     }
     cp_async_commit();
   };
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) issue(r_begin + s, s);
+  for (int s = 0; s < kPairStages - 1; ++s) issue(s, s);
 
-  float gm[CPL][8], fc[CPL][8], sh[CPL][8];
+  ChunkTables tb[CPL];
   int64_t frame = -1;
-  __syncthreads();  // inv_table
-
-  int stage = 0;
-  for (int64_t r = r_begin; r < r_end; ++r) {
-    issue(r + kStages - 1, stage == 0 ? kStages - 1 : stage - 1);
-    cp_async_wait<kStages - 1>();
-
-    const int64_t f = frame_of(a, r);  // the same for the whole CTA
-    if (f != frame) {
-      frame = f;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int64_t c = t + j * kThreads;
-        if (c < chunks) load_tables(a, f, c, gm[j], fc[j], sh[j]);
-      }
-    }
-
-    const uint4* buf = ring + stage * CPL * kThreads + t;
-    float2 acc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int j = 0; j < CPL; ++j)
-      if (t + j * kThreads < chunks) accumulate(buf[j * kThreads], acc);
-    const float rstd = rstd_of(row_sum_of_squares(acc, totals, static_cast<int>(r & 1)), a.cols, a.eps);
-    if (a.row_rstd != nullptr && t == 0) a.row_rstd[r] = rstd;
-
+  FrameCursor cursor(a, r_begin);
+  auto use_frame = [&](int64_t f) {  // CTA-uniform
+    if (f == frame) return;
+    frame = f;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
       const int64_t c = t + j * kThreads;
-      if (j * kThreads >= chunks) break;  // CTA-uniform
-      emit_chunk(a, r, c, c < chunks, buf[j * kThreads], rstd, gm[j], fc[j], sh[j], gsf, inv_table);
+      if (c < chunks) load_tables(a, f, c, tb[j]);
     }
-    stage = stage == kStages - 1 ? 0 : stage + 1;
+  };
+  // Skewed pipeline: in the iteration for pair p the threads form the partial
+  // sums of pair p+1 and, in the same stretch between barriers, modulate and
+  // quantize pair p; one barrier per iteration publishes pair p+1's warp
+  // totals, so the latency of the reduction and of rstd overlaps work.
+  auto partial_sums = [&](int64_t p, int s) {  // pass 1 of pair p from stage s
+    const int64_t r0 = r_begin + 2 * p;
+    const bool has1 = r0 + 1 < r_end;
+    const uint4* buf = ring + s * 2 * CPL * kThreads + t;
+    float2 acc[2][4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      if (t + j * kThreads < chunks) {
+        accumulate(buf[j * kThreads], acc[0]);
+        if (has1) accumulate(buf[(CPL + j) * kThreads], acc[1]);
+      }
+    }
+    post_totals<2>(acc, totals, static_cast<int>(p & 1));
+  };
+  auto statistics = [&](int64_t p, float (&rstd)[2]) {  // after the barrier
+    float ss[2];
+    gather_totals<2>(totals, static_cast<int>(p & 1), ss);
+    rstd[0] = rstd_of(ss[0], a.cols, a.eps);
+    rstd[1] = rstd_of(ss[1], a.cols, a.eps);
+  };
+
+  float rstd[2] = {0.0f, 0.0f};
+  if (pairs > 0) {
+    cp_async_wait<kPairStages - 2>();  // pair 0 landed
+    partial_sums(0, 0);
+  }
+  __syncthreads();  // inv_table, pair 0's totals
+  if (pairs > 0) statistics(0, rstd);
+
+  int stage = 0;
+  for (int64_t p = 0; p < pairs; ++p) {
+    const int next = stage == kPairStages - 1 ? 0 : stage + 1;
+    issue(p + kPairStages - 1, stage == 0 ? kPairStages - 1 : stage - 1);
+    cp_async_wait<kPairStages - 2>();  // pair p+1 landed
+    const bool more = p + 1 < pairs;   // CTA-uniform
+    if (more) partial_sums(p + 1, next);
+
+    const int64_t r0 = r_begin + 2 * p;
+    const bool has1 = r0 + 1 < r_end;  // CTA-uniform
+    const uint4* buf = ring + stage * 2 * CPL * kThreads + t;
+    if (a.row_rstd != nullptr && t == 0) {
+      a.row_rstd[r0] = rstd[0];
+      if (has1) a.row_rstd[r0 + 1] = rstd[1];
+    }
+    uint8_t* code_base[2];
+    uint8_t* scale_base[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      code_base[k] = a.codes + (r0 + k) * (a.cols >> 1) + t * 4;
+      scale_base[k] = a.scales + scale_row_offset(r0 + k, quads) + (t >> 3) * 512;
+    }
+    const int64_t f0 = cursor.at(a, r0);
+    const int64_t f1 = has1 ? cursor.at(a, r0 + 1) : f0;
+    if (has1 && f0 == f1) {
+      use_frame(f0);
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        if (j * kThreads >= chunks) break;  // CTA-uniform
+        const uint4 v[2] = {buf[j * kThreads], buf[(CPL + j) * kThreads]};
+        uint8_t* const ca[2] = {code_base[0] + j * 512, code_base[1] + j * 512};
+        uint8_t* const sa[2] = {scale_base[0] + j * 8192, scale_base[1] + j * 8192};
+        emit_chunk<2>(v, rstd, tb[j], t + j * kThreads < chunks, ca, sa, gsf, inv_table);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k == 1 && !has1) break;
+        use_frame(k == 0 ? f0 : f1);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          if (j * kThreads >= chunks) break;
+          const uint4 v[1] = {buf[(k * CPL + j) * kThreads]};
+          const float rs[1] = {rstd[k]};
+          uint8_t* const ca[1] = {code_base[k] + j * 512};
+          uint8_t* const sa[1] = {scale_base[k] + j * 8192};
+          emit_chunk<1>(v, rs, tb[j], t + j * kThreads < chunks, ca, sa, gsf, inv_table);
+        }
+      }
+    }
+    __syncthreads();  // pair p+1's totals
+    if (more) statistics(p + 1, rstd);
+    stage = next;
   }
   cp_async_wait<0>();
   zero_padding_rows(a);
 }
-
 
 // Any width: the same chunk-to-thread mapping and order, x read from global
 // memory in both passes (the second read mostly hits L2) and the tables read
 // per chunk and row.
 __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs a) {
   __shared__ float inv_table[128];
-  __shared__ float totals[2][4];
+  __shared__ float totals[2][1][4];
   const float gsf = *a.gsf;
   fill_inverse_scales(inv_table, gsf);
   __syncthreads();
 
   const int t = threadIdx.x;
   const int64_t chunks = a.cols >> 3;
+  const int64_t quads = a.cols >> 6;
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
   const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
   for (int64_t r = r_begin; r < r_end; ++r) {
     const int64_t f = frame_of(a, r);
     const uint16_t* xr = a.x + r * a.ld;
-    float2 acc[4];
+    float2 acc[1][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    for (int64_t c = t; c < chunks; c += kThreads) accumulate(load16_stream(xr + c * 8), acc);
-    const float rstd = rstd_of(row_sum_of_squares(acc, totals, static_cast<int>(r & 1)), a.cols, a.eps);
-    if (a.row_rstd != nullptr && t == 0) a.row_rstd[r] = rstd;
+    for (int i = 0; i < 4; ++i) acc[0][i] = make_float2(0.0f, 0.0f);
+    for (int64_t c = t; c < chunks; c += kThreads) accumulate(load16_stream(xr + c * 8), acc[0]);
+    float ss[1];
+    row_sums<1>(acc, totals, static_cast<int>(r & 1), ss);
+    const float rstd[1] = {rstd_of(ss[0], a.cols, a.eps)};
+    if (a.row_rstd != nullptr && t == 0) a.row_rstd[r] = rstd[0];
     for (int64_t c0 = 0; c0 < chunks; c0 += kThreads) {  // CTA-uniform trip count
       const int64_t c = c0 + t;
       const bool valid = c < chunks;
-      float gm[8], fc[8], sh[8];
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      ChunkTables tb;
+      uint4 v[1] = {make_uint4(0u, 0u, 0u, 0u)};
       if (valid) {
-        v = load16_reused(xr + c * 8);
-        load_tables(a, f, c, gm, fc, sh);
+        v[0] = load16_reused(xr + c * 8);
+        load_tables(a, f, c, tb);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) gm[i] = fc[i] = sh[i] = 0.0f;
+        for (int i = 0; i < 4; ++i) {
+          tb.gm[i] = tb.fc[i] = make_float2(0.0f, 0.0f);
+          tb.sh[i] = 0u;
+        }
       }
-      emit_chunk(a, r, c, valid, v, rstd, gm, fc, sh, gsf, inv_table);
+      uint8_t* const ca[1] = {a.codes + r * (a.cols >> 1) + c * 4};
+      uint8_t* const sa[1] = {a.scales + scale_row_offset(r, quads) + (c >> 3) * 512};
+      emit_chunk<1>(v, rstd, tb, valid, ca, sa, gsf, inv_table);
     }
   }
   zero_padding_rows(a);
@@ -296,7 +455,7 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
 
 template <int CPL>
 cudaError_t launch_resident(const AdalnArgs& a, cudaStream_t stream) {
-  const int smem = kStages * CPL * kThreads * 16;
+  const int smem = kPairStages * 2 * CPL * kThreads * 16;
   int blocks = 0;
   cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_kernel<CPL>), kThreads,
                                       smem, a.rows > 0 ? a.rows : 1, &blocks);

@@ -119,7 +119,7 @@ cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, i
   if (per_sm == 0) {
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (err != cudaSuccess) return err;
-    if (smem_bytes > 48 * 1024) {
+    if (smem_bytes > 0) {  // the default limit leaves no room beside static shared memory
       err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
       if (err != cudaSuccess) return err;
     }

@@ -58,6 +58,52 @@ __device__ __forceinline__ void store_word(uint8_t* p, uint32_t v) {
 // Number formats
 // ---------------------------------------------------------------------------
 
+// Paired binary32 arithmetic, each lane rounded to nearest even on its own.
+// A paired multiply followed by a paired add of its result is contracted into a
+// fused multiply-add by the code generator even with an explicit .rn and
+// -fmad=false (a one-ulp difference from the separately rounded sequence, seen
+// on rare elements of full-size outputs).  The kernels therefore never feed the
+// result of mul2 into add2: such adds are done with scalar add.rn.f32 (or the
+// mixed bf16 form below), which are not contracted.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// Paired fused multiply-add a * b + c with one rounding per lane.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// fl(b + c) for each half b of a bf16 pair and fp32 c (scalar add.rn, bf16
+// operand taken as is): (lo + c.x, hi + c.y).
+__device__ __forceinline__ float2 add_bf16x2_f32(uint32_t b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(b), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 // bf16 pair (low half = element 2i, high half = element 2i+1) -> two fp32.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -159,8 +205,8 @@ __device__ __forceinline__ uint32_t block_scale(float amax, float gsf) {
 // Codes of eight bf16 values (four words) under the inverse scale inv.
 __device__ __forceinline__ uint32_t codes8(const uint32_t* w, float inv) {
   const float2 inv2 = make_float2(inv, inv);
-  return e2m1x8(__fmul2_rn(bf16x2_to_float2(w[0]), inv2), __fmul2_rn(bf16x2_to_float2(w[1]), inv2),
-                __fmul2_rn(bf16x2_to_float2(w[2]), inv2), __fmul2_rn(bf16x2_to_float2(w[3]), inv2));
+  return e2m1x8(mul2(bf16x2_to_float2(w[0]), inv2), mul2(bf16x2_to_float2(w[1]), inv2),
+                mul2(bf16x2_to_float2(w[2]), inv2), mul2(bf16x2_to_float2(w[3]), inv2));
 }
 
 struct Quantized {

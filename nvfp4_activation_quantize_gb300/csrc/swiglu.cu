@@ -65,26 +65,27 @@ __device__ __forceinline__ float2 exp_neg2(float2 g) {
     gc.x = fminf(fmaxf(g.x, -89.0f), 104.0f);
     gc.y = fminf(fmaxf(g.y, -89.0f), 104.0f);
   }
-  const float2 t = __fmul2_rn(gc, splat(-kL2E));
-  const float2 m = __fadd2_rn(t, splat(kRound));
-  const float2 k = __fadd2_rn(m, splat(-kRound));
-  float2 r = __ffma2_rn(k, splat(kC1), gc);
-  r = __ffma2_rn(k, splat(kC2), r);
+  const float2 t = mul2(gc, splat(-kL2E));
+  // scalar adds: a paired add of a paired product would be contracted
+  const float2 m = make_float2(__fadd_rn(t.x, kRound), __fadd_rn(t.y, kRound));
+  const float2 k = add2(m, splat(-kRound));
+  float2 r = fma2(k, splat(kC1), gc);
+  r = fma2(k, splat(kC2), r);
   float2 p = splat(-kP7);
-  p = __ffma2_rn(p, r, splat(kP6));
-  p = __ffma2_rn(p, r, splat(-kP5));
-  p = __ffma2_rn(p, r, splat(kP4));
-  p = __ffma2_rn(p, r, splat(-kP3));
-  p = __ffma2_rn(p, r, splat(kP2));
-  p = __ffma2_rn(p, r, splat(-1.0f));
-  p = __ffma2_rn(p, r, splat(1.0f));
+  p = fma2(p, r, splat(kP6));
+  p = fma2(p, r, splat(-kP5));
+  p = fma2(p, r, splat(kP4));
+  p = fma2(p, r, splat(-kP3));
+  p = fma2(p, r, splat(kP2));
+  p = fma2(p, r, splat(-1.0f));
+  p = fma2(p, r, splat(1.0f));
   if (FAST) {
     // 2^k is a normal binary32; its exponent field is k + 127, and k itself sits
     // in the low bits of m (spacing 1 around 1.5 * 2^23).
     const int kx = __float_as_int(m.x) - __float_as_int(kRound);
     const int ky = __float_as_int(m.y) - __float_as_int(kRound);
     const float2 s = make_float2(__int_as_float((kx + 127) << 23), __int_as_float((ky + 127) << 23));
-    return __fmul2_rn(p, s);
+    return mul2(p, s);
   }
   // k in [-150, 128]: ldexpf scales exactly and rounds once (into the subnormal
   // range or to infinity), which is fl(p * 2^k).
@@ -103,10 +104,12 @@ __device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u,
     const float2 gv = bf16x2_to_float2(g.w[i]);
     const float2 uv = bf16x2_to_float2(u.w[i]);
     const float2 e = exp_neg2<FAST>(gv);
-    const float2 d = __fadd2_rn(splat(1.0f), e);
+    // e = p * 2^k is exact except below 2^-126, where 1 + e rounds to 1 either
+    // way, so even a fused form of this add would give the same d
+    const float2 d = add2(splat(1.0f), e);
     const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
-    const float2 s = __fmul2_rn(gv, sig);
-    y.w[i] = float2_to_bf16x2(__fmul2_rn(s, uv));
+    const float2 s = mul2(gv, sig);
+    y.w[i] = float2_to_bf16x2(mul2(s, uv));
   }
 }
 

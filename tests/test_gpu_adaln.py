@@ -101,25 +101,20 @@ def test_eps_and_constant_rows(dev):
         assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))
 
 
-def test_full_65280x7168_sampled_rows(dev):
+def test_full_65280x7168_every_row(dev):
     """The 65,280 x 7,168 workload (32 frames of 2,040 tokens, per-channel LogNormal
-    scales): rows 0-255, the last 256 and 4,096 random rows, every byte of each,
-    plus rstd; the launch configuration is the benchmark's."""
+    scales) in the launch configuration the benchmark times: every byte of the codes
+    and of the swizzled scales, and every row's rstd, against the oracle."""
     w = workloads.adaln_inputs(dev)
     rows, cols = w["x"].shape
-    sample = workloads.sample_rows(rows, seed=3).numpy()
-    frames = sample // w["rows_per_frame"]
-    gsf = _oracle_gsf(w, frames, torch.as_tensor(sample, device=dev))
+    frames = np.arange(rows) // w["rows_per_frame"]
+    calib = workloads.sample_rows(rows, seed=3).numpy()
+    gsf = _oracle_gsf(w, calib // w["rows_per_frame"], torch.as_tensor(calib, device=dev))
     codes, scales, rstd = _run(dev, w, gsf, rows_per_frame=w["rows_per_frame"])
-    xs = w["x"].index_select(0, torch.as_tensor(sample, device=dev))
-    co, so, ro, _ = oracle.adaln_rows(bits(xs), bits(w["gamma"]), bits(w["table"]), frames,
+    co, so, ro, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames,
                                       w["eps"], gsf, threads=THREADS)
-    check_rows(codes, scales, sample, cols, co, so, "adaln 65280x7168")
-    got = rstd.cpu().numpy()[sample]
-    assert np.array_equal(got.view(np.uint32), ro.view(np.uint32))
-    # every output byte was written (no sentinel left) and scales are in range
-    assert not (rstd.view(torch.int32) == int(np.array(0xABABABAB, np.uint32).view(np.int32))).any()
-    assert int(scales.max()) <= 0x7E
+    check_full(codes, scales, rows, cols, co, so, "adaln 65280x7168")
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))
 
 
 def test_rstd_within_stated_tolerance_of_binary64(dev):

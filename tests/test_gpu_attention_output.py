@@ -36,20 +36,15 @@ def test_ragged_1000_tokens_every_byte(dev):
 
 
 @pytest.mark.parametrize("tokens", [65280, 300000])
-def test_sampled_rows(dev, tokens):
+def test_every_row(dev, tokens):
+    """Every byte of codes and swizzled scales against the oracle; at S = 300,000 the
+    tensor holds 2,150,400,000 elements, so rows past 2^31 elements are included."""
     x = workloads.attention_output(dev, tokens=tokens)
     assert x.numel() > 2**31 or tokens < 299593
     gsf = oracle.global_scale(float(x.abs().max().float()))
     codes = fill(torch.empty((tokens, 3584), dtype=torch.uint8, device=dev))
     scales = fill(torch.empty((h3q.padded_rows(tokens), 448), dtype=torch.uint8, device=dev))
     h3q.h3q_quantize_nvfp4(x, gsf_tensor(gsf, dev), codes, scales)
-    sample = workloads.sample_rows(tokens, seed=5).numpy()
-    # rows whose elements sit past 2^31 are in the tail sample for S = 300,000
-    idx = torch.as_tensor(sample, device=dev)
-    co, so = oracle.quantize_rows(bits(x.index_select(0, idx)), gsf, threads=THREADS)
-    check_rows(codes, scales, sample, 7168, co, so, f"attention output S={tokens}")
+    co, so = oracle.quantize_rows(bits(x), gsf, threads=THREADS)
+    check_full(codes, scales, tokens, 7168, co, so, f"attention output S={tokens}")
     check_padding(scales, tokens, 7168, f"attention output S={tokens}")
-    # no sentinel byte survives anywhere in either output
-    assert not (scales == 0xAB).any()
-    tail = codes[-4096:]
-    assert not (tail == 0xAB).all(dim=1).any()

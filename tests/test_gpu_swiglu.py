@@ -92,18 +92,14 @@ def test_packed_gate_up_projection_views(dev):
     check_full(codes, scales, rows, f, co, so, "packed projection")
 
 
-def test_full_65280x18944_sampled_rows(dev):
+def test_full_65280x18944_every_row(dev):
     """The 65,280 x 18,944 workload, gate and up ~ N(0, 1.5^2); gsf from a
-    calibration pass of the oracle over 2,048 rows of the same seed; rows 0-255,
-    the last 256 and 4,096 random rows compared byte for byte."""
+    calibration pass of the oracle over 2,048 rows of the same seed; every byte of
+    the codes and of the swizzled scales against the oracle."""
     gate, up = workloads.swiglu_inputs(dev)
     rows, cols = gate.shape
     calib = torch.arange(0, rows, rows // 2048, device=dev)[:2048]
     gsf = _oracle_gsf(gate.index_select(0, calib), up.index_select(0, calib))
     codes, scales = _run(dev, gate, up, gsf)
-    sample = workloads.sample_rows(rows, seed=4).numpy()
-    idx = torch.as_tensor(sample, device=dev)
-    co, so, _ = oracle.swiglu_rows(bits(gate.index_select(0, idx)), bits(up.index_select(0, idx)),
-                                   gsf, threads=THREADS)
-    check_rows(codes, scales, sample, cols, co, so, "swiglu 65280x18944")
-    assert int(scales.max()) <= 0x7E
+    co, so, _ = oracle.swiglu_rows(bits(gate), bits(up), gsf, threads=THREADS)
+    check_full(codes, scales, rows, cols, co, so, "swiglu 65280x18944")
