@@ -304,7 +304,7 @@ def run_ours(args, rank, world, dev):
             "traffic": recorded_traffic("adaln_kernel"),
             "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "kernel": "adaln_kernel<14>",
+            "kernel": "adaln_kernel<7>",
             "launch_ms": round(launch_ms, 5),
         },
         "gpu_launches": args.steps,

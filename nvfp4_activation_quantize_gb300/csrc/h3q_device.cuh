@@ -104,6 +104,24 @@ __device__ __forceinline__ float2 add_bf16x2_f32(uint32_t b, float2 c) {
   return r;
 }
 
+// fl(1 / d) for two d in [1, 2^126): a hardware reciprocal estimate refined by
+// one Newton-Raphson step and Markstein's final correction (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Dev. 34(1), 1990): e = 1 - d*y, y' = y + y*e, twice, with fused
+// multiply-adds; the last step rounds to the correctly rounded reciprocal.
+// Equal to __frcp_rn for every binary32 d in [1, 2^126) (checked exhaustively
+// on the GPU by tests/test_gpu_device_identities.py).
+__device__ __forceinline__ float2 rcp_rn_ge1(float2 d) {
+  float2 y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.x) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.y) : "f"(d.y));
+  const float2 nd = mul2(d, make_float2(-1.0f, -1.0f));
+  float2 e = fma2(nd, y, make_float2(1.0f, 1.0f));
+  y = fma2(y, e, y);
+  e = fma2(nd, y, make_float2(1.0f, 1.0f));
+  return fma2(y, e, y);
+}
+
 // bf16 pair (low half = element 2i, high half = element 2i+1) -> two fp32.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -175,7 +193,7 @@ __device__ __forceinline__ float block_amax(const Block16& y) {
 // fl(a / 6) for a bf16 value a >= 0 without a division: q0 = fl(a * fl(1/6)) is
 // corrected once by its exact remainder.  Equal to the correctly rounded
 // quotient for every finite such a (checked over all of them in exact
-// arithmetic); +inf (a bf16 overflow of y) is passed through as inf / 6 = inf.
+// arithmetic, and against the hardware division on the GPU); +inf (a bf16 overflow of y) is passed through as inf / 6 = inf.
 __device__ __forceinline__ float amax_over_six(float a) {
   constexpr float kR6 = 0x1.555556p-3f;  // fl(1/6)
   const float q0 = __fmul_rn(a, kR6);

@@ -107,7 +107,8 @@ __device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u,
     // e = p * 2^k is exact except below 2^-126, where 1 + e rounds to 1 either
     // way, so even a fused form of this add would give the same d
     const float2 d = add2(splat(1.0f), e);
-    const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    // FAST: |g| <= 87, so d = 1 + e lies in [1, 2^126)
+    const float2 sig = FAST ? rcp_rn_ge1(d) : make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
     const float2 s = mul2(gv, sig);
     y.w[i] = float2_to_bf16x2(mul2(s, uv));
   }

@@ -1,0 +1,27 @@
+"""The kernels' division-free routines against CUDA's correctly rounded operations,
+exhaustively on the GPU: the Markstein reciprocal used for the SiLU sigmoid over
+every binary32 in [1, 2^126), and the once-corrected fl(a/6) of the block scale
+over every bf16 value (tests/device/identities.cu, compiled here with the
+library's own flags)."""
+import os
+import subprocess
+
+import pytest
+import torch
+
+from nvfp4_activation_quantize_gb300 import build as libbuild
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_division_free_routines_match_cuda(tmp_path):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    exe = str(tmp_path / "identities")
+    flags = [f for f in libbuild.NVCC_FLAGS if f not in ("-Xcompiler", "-fPIC", "-Xptxas", "-v")]
+    subprocess.run([libbuild._nvcc(), *flags, os.path.join(HERE, "device", "identities.cu"), "-o", exe],
+                   check=True)
+    res = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "rcp_rn_ge1 mismatches 0" in res.stdout and "amax_over_six mismatches 0" in res.stdout
