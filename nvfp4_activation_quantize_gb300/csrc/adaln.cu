@@ -35,7 +35,8 @@
 namespace h3q {
 namespace {
 
-constexpr int kThreads = 128;  // the lanes of the canonical order
+constexpr int kThreads = 128;   // CTA size of the generic kernel
+constexpr int kLanes128 = 128;  // the lanes of the canonical order
 constexpr int kPairStages = 3;  // row pairs of x per CTA in the cp.async ring
 
 struct AdalnArgs {
@@ -183,8 +184,8 @@ __device__ __forceinline__ void row_sums(const float2 (&acc)[R][4], float (*tota
   gather_totals<R>(totals, slot, ss);
 }
 
-__device__ __forceinline__ float rstd_of(float ss, int64_t cols, float eps) {
-  const float mean = __fdiv_rn(ss, static_cast<float>(cols));
+__device__ __forceinline__ float rstd_of(float ss, float cols, float eps) {
+  const float mean = __fdiv_rn(ss, cols);
   return __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
 }
 
@@ -196,9 +197,9 @@ __device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
 
 // Modulate one chunk of R rows (x words v[k], statistics rstd[k]) with the
 // chunk's tables, quantize this thread's half block of each row, store its four
-// code bytes at codes_at[k] and, from the first lane of each group of eight,
-// the scale word of the group's four blocks at scale_at[k].  All 32 lanes of
-// the warp call this (it shuffles); `valid` masks the stores.
+// code bytes at codes_at[k] and, from the even thread of the pair, the block's
+// scale byte at scale_at[k].  All 32 lanes of the warp call this (it
+// shuffles); `valid` masks the stores.
 template <int R>
 __device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rstd)[R],
                                            const ChunkTables& tb, bool valid,
@@ -228,21 +229,14 @@ __device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rs
                                         absmax_bf16x2(y[k][2], y[k][3])));
 #pragma unroll
   for (int k = 0; k < R; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], 1));
-  uint32_t sf[R], word[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    sf[k] = block_scale(amax[k], gsf);
-    const uint32_t codes = codes8(y[k], inv_table[sf[k]]);
+    const uint32_t sf = block_scale(amax[k], gsf);
+    const uint32_t codes = codes8(y[k], inv_table[sf]);
     if (valid) store_word(codes_at[k], codes);
-    word[k] = (lane & 1) ? 0u : sf[k] << (8 * ((lane >> 1) & 3));
+    // the even thread of the pair writes the block's scale byte
+    if (valid && !(lane & 1)) store_byte(scale_at[k], sf);
   }
-#pragma unroll
-  for (int k = 0; k < R; ++k) word[k] |= __shfl_xor_sync(0xffffffffu, word[k], 2);
-#pragma unroll
-  for (int k = 0; k < R; ++k) word[k] |= __shfl_xor_sync(0xffffffffu, word[k], 4);
-  if (valid && (lane & 7) == 0)
-#pragma unroll
-    for (int k = 0; k < R; ++k) store_word(scale_at[k], word[k]);
 }
 
 // Zero scale words of the padding rows rows..pad128(rows)-1, spread over CTAs.
@@ -250,18 +244,26 @@ __device__ __forceinline__ void zero_padding_rows(const AdalnArgs& a) {
   const int64_t prows = (a.rows + 127) >> 7 << 7;
   const int64_t quads = a.cols >> 6;
   for (int64_t p = a.rows + blockIdx.x; p < prows; p += gridDim.x)
-    for (int64_t q = threadIdx.x; q < quads; q += kThreads)
+    for (int64_t q = threadIdx.x; q < quads; q += blockDim.x)
       store_word(a.scales + scale_word_offset(p, q, quads), 0u);
 }
 
-// Rows up to 128 * CPL chunks (CPL * 1,024 columns): tables resident in
-// registers, x through a cp.async ring in dynamic shared memory laid out as
-// [kPairStages][2][CPL][128] 16-byte chunks (each warp's 32 chunks contiguous).
-// Rows go in consecutive pairs: one barrier per pair, and the two rows'
-// independent arithmetic interleaves under the same table registers.  A pair
-// whose rows lie in different frames is emitted one row at a time.
-template <int CPL>
-__global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
+// Rows up to 128 * C1 chunks (C1 * 1,024 columns), with NT threads per CTA.
+// Pass 1 runs on threads 0..127, the lanes of the canonical order, C1 chunks
+// each (chunk c on lane c % 128).  Pass 2 is element-wise, so it spreads the
+// row over all NT threads, J chunks each (chunk c on thread c % NT); a thread
+// keeps the tables of its J chunks in registers (gamma and 1 + scale as fp32
+// pairs, the shift as bf16 pairs), so more threads mean fewer registers each.
+// x streams through a cp.async ring in dynamic shared memory,
+// [kPairStages][2 rows][128 * C1 chunks] of 16 bytes, copied by the pass-1
+// lanes chunk by chunk as they will read it.  Rows go in consecutive pairs
+// with a skewed pipeline: the iteration for pair p forms the partial sums of
+// pair p+1 and modulates and quantizes pair p, then one barrier publishes
+// pair p+1's warp totals.  Pass 2 of pair p reads chunks copied by other
+// threads; every thread's wait for pair p came before the previous barrier.
+template <int NT, int J, int C1, bool FULL>
+__global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
+  constexpr int kRow = kLanes128 * C1;  // chunk slots per row in the ring
   extern __shared__ uint4 ring[];
   __shared__ float inv_table[128];
   __shared__ float totals[2][2][4];
@@ -269,27 +271,32 @@ __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
   fill_inverse_scales(inv_table, gsf);
 
   const int t = threadIdx.x;
+  const bool lane1 = t < kLanes128;  // a pass-1 lane (warp-uniform)
   const int64_t chunks = a.cols >> 3;
   const int64_t quads = a.cols >> 6;
+  const float cols_f = static_cast<float>(a.cols);  // exact: cols <= 2^24
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
   const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
   const int64_t pairs = (r_end - r_begin + 1) >> 1;
   const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
-  // Copy this thread's chunks of pair p into ring stage s; always commit a
-  // group (empty past the range) so that group counting stays uniform.
-  const uint16_t* x_t = a.x + t * 8;                      // this thread's first chunk
+  // The pass-1 lanes copy their chunks of pair p into ring stage s; every
+  // thread commits a group (empty for the others and past the range).
+  const uint16_t* x_t = a.x + t * 8;
   const uint32_t ring_t = ring_base + t * 16;
   auto issue = [&](int64_t p, int s) {
+    if (lane1) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int64_t r = r_begin + 2 * p + k;
-      if (r < r_end) {
-        const uint16_t* xr = x_t + r * a.ld;
-        const uint32_t dst = ring_t + (s * 2 + k) * (CPL * kThreads * 16);
+      for (int k = 0; k < 2; ++k) {
+        const int64_t r = r_begin + 2 * p + k;
+        if (r < r_end) {
+          const uint16_t* xr = x_t + r * a.ld;
+          const uint32_t dst = ring_t + (s * 2 + k) * (kRow * 16);
 #pragma unroll
-        for (int j = 0; j < CPL; ++j)
-          if (t + j * kThreads < chunks) cp_async16(dst + j * (kThreads * 16), xr + j * (kThreads * 8));
+          for (int j = 0; j < C1; ++j)
+            if (FULL || t + j * kLanes128 < chunks)
+              cp_async16(dst + j * (kLanes128 * 16), xr + j * (kLanes128 * 8));
+        }
       }
     }
     cp_async_commit();
@@ -297,36 +304,34 @@ __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
 #pragma unroll
   for (int s = 0; s < kPairStages - 1; ++s) issue(s, s);
 
-  ChunkTables tb[CPL];
+  ChunkTables tb[J];
   int64_t frame = -1;
   FrameCursor cursor(a, r_begin);
   auto use_frame = [&](int64_t f) {  // CTA-uniform
     if (f == frame) return;
     frame = f;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int64_t c = t + j * kThreads;
-      if (c < chunks) load_tables(a, f, c, tb[j]);
+    for (int j = 0; j < J; ++j) {
+      const int64_t c = t + j * NT;
+      if (FULL || c < chunks) load_tables(a, f, c, tb[j]);
     }
   };
-  // Skewed pipeline: in the iteration for pair p the threads form the partial
-  // sums of pair p+1 and, in the same stretch between barriers, modulate and
-  // quantize pair p; one barrier per iteration publishes pair p+1's warp
-  // totals, so the latency of the reduction and of rstd overlaps work.
-  auto partial_sums = [&](int64_t p, int s) {  // pass 1 of pair p from stage s
+
+  auto partial_sums = [&](int64_t p, int s) {  // pass 1 of pair p from stage s (lanes only)
+    if (!lane1) return;
     const int64_t r0 = r_begin + 2 * p;
     const bool has1 = r0 + 1 < r_end;
-    const uint4* buf = ring + s * 2 * CPL * kThreads + t;
+    const uint4* buf = ring + s * 2 * kRow + t;
     float2 acc[2][4];
 #pragma unroll
     for (int k = 0; k < 2; ++k)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      if (t + j * kThreads < chunks) {
-        accumulate(buf[j * kThreads], acc[0]);
-        if (has1) accumulate(buf[(CPL + j) * kThreads], acc[1]);
+    for (int j = 0; j < C1; ++j) {
+      if (FULL || t + j * kLanes128 < chunks) {
+        accumulate(buf[j * kLanes128], acc[0]);
+        if (has1) accumulate(buf[kRow + j * kLanes128], acc[1]);
       }
     }
     post_totals<2>(acc, totals, static_cast<int>(p & 1));
@@ -334,29 +339,29 @@ __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
   auto statistics = [&](int64_t p, float (&rstd)[2]) {  // after the barrier
     float ss[2];
     gather_totals<2>(totals, static_cast<int>(p & 1), ss);
-    rstd[0] = rstd_of(ss[0], a.cols, a.eps);
-    rstd[1] = rstd_of(ss[1], a.cols, a.eps);
+    rstd[0] = rstd_of(ss[0], cols_f, a.eps);
+    rstd[1] = rstd_of(ss[1], cols_f, a.eps);
   };
 
   float rstd[2] = {0.0f, 0.0f};
   if (pairs > 0) {
-    cp_async_wait<kPairStages - 2>();  // pair 0 landed
+    cp_async_wait<kPairStages - 2>();  // pair 0 landed (this thread's copies)
     partial_sums(0, 0);
   }
-  __syncthreads();  // inv_table, pair 0's totals
+  __syncthreads();  // inv_table, pair 0's totals, every thread's pair-0 copies
   if (pairs > 0) statistics(0, rstd);
 
   int stage = 0;
   for (int64_t p = 0; p < pairs; ++p) {
     const int next = stage == kPairStages - 1 ? 0 : stage + 1;
     issue(p + kPairStages - 1, stage == 0 ? kPairStages - 1 : stage - 1);
-    cp_async_wait<kPairStages - 2>();  // pair p+1 landed
+    cp_async_wait<kPairStages - 2>();  // pair p+1 landed (this thread's copies)
     const bool more = p + 1 < pairs;   // CTA-uniform
     if (more) partial_sums(p + 1, next);
 
     const int64_t r0 = r_begin + 2 * p;
     const bool has1 = r0 + 1 < r_end;  // CTA-uniform
-    const uint4* buf = ring + stage * 2 * CPL * kThreads + t;
+    const uint4* buf = ring + stage * 2 * kRow + t;
     if (a.row_rstd != nullptr && t == 0) {
       a.row_rstd[r0] = rstd[0];
       if (has1) a.row_rstd[r0 + 1] = rstd[1];
@@ -366,19 +371,19 @@ __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       code_base[k] = a.codes + (r0 + k) * (a.cols >> 1) + t * 4;
-      scale_base[k] = a.scales + scale_row_offset(r0 + k, quads) + (t >> 3) * 512;
+      scale_base[k] = a.scales + scale_row_offset(r0 + k, quads) + (t >> 3) * 512 + ((t >> 1) & 3);
     }
     const int64_t f0 = cursor.at(a, r0);
     const int64_t f1 = has1 ? cursor.at(a, r0 + 1) : f0;
     if (has1 && f0 == f1) {
       use_frame(f0);
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        if (j * kThreads >= chunks) break;  // CTA-uniform
-        const uint4 v[2] = {buf[j * kThreads], buf[(CPL + j) * kThreads]};
-        uint8_t* const ca[2] = {code_base[0] + j * 512, code_base[1] + j * 512};
-        uint8_t* const sa[2] = {scale_base[0] + j * 8192, scale_base[1] + j * 8192};
-        emit_chunk<2>(v, rstd, tb[j], t + j * kThreads < chunks, ca, sa, gsf, inv_table);
+      for (int j = 0; j < J; ++j) {
+        if (!FULL && j * NT >= chunks) break;  // CTA-uniform
+        const uint4 v[2] = {buf[j * NT], buf[kRow + j * NT]};
+        uint8_t* const ca[2] = {code_base[0] + j * (NT * 4), code_base[1] + j * (NT * 4)};
+        uint8_t* const sa[2] = {scale_base[0] + j * (NT / 8 * 512), scale_base[1] + j * (NT / 8 * 512)};
+        emit_chunk<2>(v, rstd, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table);
       }
     } else {
 #pragma unroll
@@ -386,17 +391,17 @@ __global__ void __launch_bounds__(kThreads, 2) adaln_kernel(const AdalnArgs a) {
         if (k == 1 && !has1) break;
         use_frame(k == 0 ? f0 : f1);
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          if (j * kThreads >= chunks) break;
-          const uint4 v[1] = {buf[(k * CPL + j) * kThreads]};
+        for (int j = 0; j < J; ++j) {
+          if (!FULL && j * NT >= chunks) break;
+          const uint4 v[1] = {buf[k * kRow + j * NT]};
           const float rs[1] = {rstd[k]};
-          uint8_t* const ca[1] = {code_base[k] + j * 512};
-          uint8_t* const sa[1] = {scale_base[k] + j * 8192};
-          emit_chunk<1>(v, rs, tb[j], t + j * kThreads < chunks, ca, sa, gsf, inv_table);
+          uint8_t* const ca[1] = {code_base[k] + j * (NT * 4)};
+          uint8_t* const sa[1] = {scale_base[k] + j * (NT / 8 * 512)};
+          emit_chunk<1>(v, rs, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table);
         }
       }
     }
-    __syncthreads();  // pair p+1's totals
+    __syncthreads();  // pair p+1's totals and every thread's pair-(p+1) copies
     if (more) statistics(p + 1, rstd);
     stage = next;
   }
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
     for (int64_t c = t; c < chunks; c += kThreads) accumulate(load16_stream(xr + c * 8), acc[0]);
     float ss[1];
     row_sums<1>(acc, totals, static_cast<int>(r & 1), ss);
-    const float rstd[1] = {rstd_of(ss[0], a.cols, a.eps)};
+    const float rstd[1] = {rstd_of(ss[0], static_cast<float>(a.cols), a.eps)};
     if (a.row_rstd != nullptr && t == 0) a.row_rstd[r] = rstd[0];
     for (int64_t c0 = 0; c0 < chunks; c0 += kThreads) {  // CTA-uniform trip count
       const int64_t c = c0 + t;
@@ -446,21 +451,26 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
         }
       }
       uint8_t* const ca[1] = {a.codes + r * (a.cols >> 1) + c * 4};
-      uint8_t* const sa[1] = {a.scales + scale_row_offset(r, quads) + (c >> 3) * 512};
+      uint8_t* const sa[1] = {a.scales + scale_row_offset(r, quads) + (c >> 3) * 512 + ((c >> 1) & 3)};
       emit_chunk<1>(v, rstd, tb, valid, ca, sa, gsf, inv_table);
     }
   }
   zero_padding_rows(a);
 }
 
-template <int CPL>
+template <int NT, int J, int C1>
 cudaError_t launch_resident(const AdalnArgs& a, cudaStream_t stream) {
-  const int smem = kPairStages * 2 * CPL * kThreads * 16;
+  const int smem = kPairStages * 2 * kLanes128 * C1 * 16;
+  const bool full = a.cols / 8 == int64_t(NT) * J && a.cols / 8 == int64_t(kLanes128) * C1;
+  const void* kernel = full ? reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, true>)
+                            : reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, false>);
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_kernel<CPL>), kThreads,
-                                      smem, a.rows > 0 ? a.rows : 1, &blocks);
+  cudaError_t err = persistent_blocks(kernel, NT, smem, a.rows > 0 ? a.rows : 1, &blocks);
   if (err != cudaSuccess) return err;
-  adaln_kernel<CPL><<<blocks, kThreads, smem, stream>>>(a);
+  if (full)
+    adaln_kernel<NT, J, C1, true><<<blocks, NT, smem, stream>>>(a);
+  else
+    adaln_kernel<NT, J, C1, false><<<blocks, NT, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -482,12 +492,13 @@ cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                          cudaStream_t stream) {
   const AdalnArgs a{x,    ld,   gamma, table, num_frames, row_frame, rows_per_frame,
                     eps,  rows, cols,  gsf,   codes,      scales,    row_rstd};
-  const int64_t per_thread = (cols / 8 + kThreads - 1) / kThreads;  // chunks per thread
-  if (per_thread <= 1) return launch_resident<1>(a, stream);
-  if (per_thread <= 2) return launch_resident<2>(a, stream);
-  if (per_thread <= 4) return launch_resident<4>(a, stream);
-  if (per_thread <= 7) return launch_resident<7>(a, stream);
-  if (per_thread <= 8) return launch_resident<8>(a, stream);
+  const int64_t chunks = cols / 8;
+  const int64_t per_lane = (chunks + kLanes128 - 1) / kLanes128;
+  if (per_lane <= 1) return launch_resident<128, 1, 1>(a, stream);
+  if (per_lane <= 2) return launch_resident<128, 2, 2>(a, stream);
+  if (per_lane <= 4) return launch_resident<128, 4, 4>(a, stream);
+  if (per_lane <= 7) return launch_resident<128, 7, 7>(a, stream);
+  if (per_lane <= 8) return launch_resident<128, 8, 8>(a, stream);
   return launch_generic(a, stream);
 }
 

@@ -50,6 +50,10 @@ __device__ __forceinline__ void store_codes(uint8_t* p, uint32_t lo, uint32_t hi
   asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
 }
 
+__device__ __forceinline__ void store_byte(uint8_t* p, uint32_t v) {
+  asm volatile("st.global.b8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void store_word(uint8_t* p, uint32_t v) {
   asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
