@@ -135,12 +135,16 @@ __device__ __forceinline__ void load_tables(const AdalnArgs& a, int64_t t, int64
 }
 
 // Partials (p_2i, p_2i+1) in acc[i]; element e of the chunk goes to p_e.
+// The squares come from the bf16 halves directly (fma.rn.f32.bf16: exact
+// product of two bf16 values, one rounding with the fp32 partial).
 __device__ __forceinline__ void accumulate(const uint4& v, float2 (&acc)[4]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = bf16x2_to_float2(w[i]);
-    acc[i] = fma2(f, f, acc[i]);
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %1, h, h, %1;\n\t}"
+        : "+f"(acc[i].x), "+f"(acc[i].y)
+        : "r"(w[i]));
   }
 }
 
