@@ -166,9 +166,9 @@ __device__ __forceinline__ void post_totals(const float2 (&acc)[R][4], float (*t
   for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
     for (int k = 0; k < R; ++k) tot[k] = __fadd_rn(tot[k], __shfl_xor_sync(0xffffffffu, tot[k], o));
-  if ((threadIdx.x & 31) == 0)
+  if ((threadIdx.x & 31) == 0)  // warp index within the 128-lane group
 #pragma unroll
-    for (int k = 0; k < R; ++k) totals[slot][k][threadIdx.x >> 5] = tot[k];
+    for (int k = 0; k < R; ++k) totals[slot][k][(threadIdx.x >> 5) & 3] = tot[k];
 }
 
 template <int R>
