@@ -195,6 +195,20 @@ def time_launches(fn, steps: int, stream, flush=None):
     return starts[0].elapsed_time(ends[-1]), per
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's elapsed milliseconds: a replica run's timed region ends
+    when its last rank ends (all-reduce MAX; the identity on one rank)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over `steps` steps in `ms`."""
+    return world * bytes_per_rank_step * steps / (ms * 1e-3) / 1e9
+
+
 def calibrate_adaln_gsf(w) -> float:
     """Global scale from max |modulated x| (torch fp32 on the GPU, a calibration
     pass outside the timed region)."""
@@ -261,12 +275,9 @@ def run_ours(args, rank, world, dev):
     sampler.stop()
     clocks = sampler.summary(soak_t0, t1)
 
-    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(elapsed.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     nbytes = adaln_bytes(ROWS, COLS, FRAMES)
-    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_gbs(nbytes, args.steps, world, total_ms)
     launch_ms = sum(per) / len(per)
     achieved = nbytes / (launch_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -322,46 +333,49 @@ def run_ours(args, rank, world, dev):
 
 
 def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
-    """The same metric through the public call with host buffers: each step copies
-    the inputs from pinned host memory, runs the producer, copies codes and scales
-    back to pinned host memory; timed with CUDA events on the stream."""
+    """The same metric through the public host-buffer call: each step copies x,
+    gamma and the modulation table from pinned host memory, runs the producer and
+    copies codes and scales back to pinned host memory.  The call pipelines the
+    copies and the producer over 8,192-row chunks on three streams; the timed
+    region (CUDA events on the caller's stream) covers every copy of the step."""
+    from nvfp4_activation_quantize_gb300.host import HostPipeline
+
     hx = w["x"].cpu().pin_memory()
     hg = w["gamma"].cpu().pin_memory()
     ht = w["table"].cpu().pin_memory()
     hc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8).pin_memory()
     hs = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8).pin_memory()
-    dx, dg, dt = torch.empty_like(w["x"]), torch.empty_like(w["gamma"]), torch.empty_like(w["table"])
-    dc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
-    ds = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
+    pipe = HostPipeline(dev, COLS, chunk_rows=8192)
 
     def step():
-        dx.copy_(hx, non_blocking=True)
-        dg.copy_(hg, non_blocking=True)
-        dt.copy_(ht, non_blocking=True)
-        h3q.h3q_rmsnorm_adaln_nvfp4(dx, dg, dt, gsf, rows_per_frame=RPF, eps=w["eps"], codes=dc,
-                                    scales=ds, stream=stream)
-        hc.copy_(dc, non_blocking=True)
-        hs.copy_(ds, non_blocking=True)
+        pipe.rmsnorm_adaln_nvfp4(hx, hg, ht, gsf, hc, hs, rows_per_frame=RPF, eps=w["eps"])
 
     with torch.cuda.stream(stream):
-        for _ in range(2):
+        for _ in range(3):
             step()
     torch.cuda.synchronize()
     steps = max(3, min(args.steps, 10))
     total_ms, _ = time_launches(step, steps, stream)
-    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(elapsed.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     nbytes = adaln_bytes(ROWS, COLS, FRAMES)
     return {
-        "value": round(world * nbytes * steps / (total_ms * 1e-3) / 1e9, 1),
+        "value": round(job_gbs(nbytes, steps, world, total_ms), 1),
         "unit": "GB/s",
         "h2d_bytes_per_step": hx.numel() * 2 + hg.numel() * 2 + ht.numel() * 2,
         "d2h_bytes_per_step": hc.numel() + hs.numel(),
         "steps": steps,
         "ms_per_step": round(total_ms / steps, 3),
+        "pipeline": {"chunk_rows": pipe.chunk_rows, "depth": pipe.depth, "streams": 3},
+        "check": e2e_matches(h3q, dev, w, gsf, hc, hs),
     }
+
+
+def e2e_matches(h3q, dev, w, gsf, hc, hs) -> bool:
+    """The host-buffer outputs equal the device-buffer call's, byte for byte."""
+    c, s = h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], gsf, rows_per_frame=RPF,
+                                       eps=w["eps"])
+    torch.cuda.synchronize()
+    return bool(torch.equal(c.cpu(), hc) and torch.equal(s.cpu(), hs))
 
 
 def measure_producers(h3q, dev, stream, args):

@@ -81,6 +81,16 @@ static inline int64_t h3q_scale_bytes(int64_t rows, int64_t cols)
 }
 /* Bytes of the packed code matrix. */
 static inline int64_t h3q_code_bytes(int64_t rows, int64_t cols) { return rows * (cols / 2); }
+/* Byte offset, in the scale matrix, of the scales of row `row0` onwards when
+ * row0 is a multiple of 128: the 512-byte atoms are laid out row-tile major, so
+ * the scales of rows [row0, row0 + n) with n a multiple of 128 (or the tensor's
+ * last rows) form one contiguous range starting here.  A call on those rows
+ * writes exactly that range, which lets a large tensor be processed in
+ * 128-row-aligned pieces. */
+static inline int64_t h3q_scale_offset_of_row_tile(int64_t row0, int64_t cols)
+{
+    return row0 / 128 * (cols / 64) * 512;
+}
 
 /*
  * (c) Standalone NVFP4 quantize, e.g. of the attention output viewed as
