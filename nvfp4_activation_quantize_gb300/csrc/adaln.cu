@@ -21,10 +21,11 @@
 // thread keeps gamma, 1+scale and shift of its own chunks in registers as fp32
 // and reloads them only when the frame changes.  Neither the modulation table
 // nor gamma is re-read per row.
-// x streams through a ring of kPairStages row pairs in shared memory filled
-// with cp.async: each thread copies exactly the chunks it will read, so the
-// data needs no barrier, only the thread's own cp.async.wait_group; two pairs
-// per CTA are in flight while one is computed.  Rows are processed in pairs,
+// x streams through a ring of row pairs in shared memory filled with cp.async:
+// each thread copies exactly the chunks it will read, so the data needs no
+// barrier, only the thread's own cp.async.wait_group.  With four pairs in the
+// ring, three are in flight or waiting while one is computed, so a pair's
+// copy is issued two iterations before its pass 1.  Rows are processed in pairs,
 // which shares one barrier and the table registers between two independent
 // rows' arithmetic.
 // Rows wider than 8,192 take a generic kernel with the same chunk-to-thread
@@ -37,7 +38,6 @@ namespace {
 
 constexpr int kThreads = 128;   // CTA size of the generic kernel
 constexpr int kLanes128 = 128;  // the lanes of the canonical order
-constexpr int kPairStages = 3;  // row pairs of x per CTA in the cp.async ring
 
 struct AdalnArgs {
   const uint16_t* x;
@@ -252,20 +252,21 @@ __device__ __forceinline__ void zero_padding_rows(const AdalnArgs& a) {
       store_word(a.scales + scale_word_offset(p, q, quads), 0u);
 }
 
-// Rows up to 128 * C1 chunks (C1 * 1,024 columns), with NT threads per CTA.
+// Rows up to 128 * C1 chunks (C1 * 1,024 columns), with NT threads per CTA and
+// S row pairs in the ring (S - 1 pairs in flight ahead of the one computed).
 // Pass 1 runs on threads 0..127, the lanes of the canonical order, C1 chunks
 // each (chunk c on lane c % 128).  Pass 2 is element-wise, so it spreads the
 // row over all NT threads, J chunks each (chunk c on thread c % NT); a thread
 // keeps the tables of its J chunks in registers (gamma and 1 + scale as fp32
 // pairs, the shift as bf16 pairs), so more threads mean fewer registers each.
 // x streams through a cp.async ring in dynamic shared memory,
-// [kPairStages][2 rows][128 * C1 chunks] of 16 bytes, copied by the pass-1
+// [S][2 rows][128 * C1 chunks] of 16 bytes, copied by the pass-1
 // lanes chunk by chunk as they will read it.  Rows go in consecutive pairs
 // with a skewed pipeline: the iteration for pair p forms the partial sums of
 // pair p+1 and modulates and quantizes pair p, then one barrier publishes
 // pair p+1's warp totals.  Pass 2 of pair p reads chunks copied by other
 // threads; every thread's wait for pair p came before the previous barrier.
-template <int NT, int J, int C1, bool FULL>
+template <int NT, int J, int C1, int S, bool FULL>
 __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
   constexpr int kRow = kLanes128 * C1;  // chunk slots per row in the ring
   extern __shared__ uint4 ring[];
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
     cp_async_commit();
   };
 #pragma unroll
-  for (int s = 0; s < kPairStages - 1; ++s) issue(s, s);
+  for (int s = 0; s < S - 1; ++s) issue(s, s);
 
   ChunkTables tb[J];
   int64_t frame = -1;
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
 
   float rstd[2] = {0.0f, 0.0f};
   if (pairs > 0) {
-    cp_async_wait<kPairStages - 2>();  // pair 0 landed (this thread's copies)
+    cp_async_wait<S - 2>();  // pair 0 landed (this thread's copies)
     partial_sums(0, 0);
   }
   __syncthreads();  // inv_table, pair 0's totals, every thread's pair-0 copies
@@ -357,9 +358,9 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
 
   int stage = 0;
   for (int64_t p = 0; p < pairs; ++p) {
-    const int next = stage == kPairStages - 1 ? 0 : stage + 1;
-    issue(p + kPairStages - 1, stage == 0 ? kPairStages - 1 : stage - 1);
-    cp_async_wait<kPairStages - 2>();  // pair p+1 landed (this thread's copies)
+    const int next = stage == S - 1 ? 0 : stage + 1;
+    issue(p + S - 1, stage == 0 ? S - 1 : stage - 1);
+    cp_async_wait<S - 2>();  // pair p+1 landed (this thread's copies)
     const bool more = p + 1 < pairs;   // CTA-uniform
     if (more) partial_sums(p + 1, next);
 
@@ -462,19 +463,19 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
   zero_padding_rows(a);
 }
 
-template <int NT, int J, int C1>
+template <int NT, int J, int C1, int S>
 cudaError_t launch_resident(const AdalnArgs& a, cudaStream_t stream) {
-  const int smem = kPairStages * 2 * kLanes128 * C1 * 16;
+  const int smem = S * 2 * kLanes128 * C1 * 16;
   const bool full = a.cols / 8 == int64_t(NT) * J && a.cols / 8 == int64_t(kLanes128) * C1;
-  const void* kernel = full ? reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, true>)
-                            : reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, false>);
+  const void* kernel = full ? reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, true>)
+                            : reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, false>);
   int blocks = 0;
   cudaError_t err = persistent_blocks(kernel, NT, smem, a.rows > 0 ? a.rows : 1, &blocks);
   if (err != cudaSuccess) return err;
   if (full)
-    adaln_kernel<NT, J, C1, true><<<blocks, NT, smem, stream>>>(a);
+    adaln_kernel<NT, J, C1, S, true><<<blocks, NT, smem, stream>>>(a);
   else
-    adaln_kernel<NT, J, C1, false><<<blocks, NT, smem, stream>>>(a);
+    adaln_kernel<NT, J, C1, S, false><<<blocks, NT, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -498,11 +499,13 @@ cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                     eps,  rows, cols,  gsf,   codes,      scales,    row_rstd};
   const int64_t chunks = cols / 8;
   const int64_t per_lane = (chunks + kLanes128 - 1) / kLanes128;
-  if (per_lane <= 1) return launch_resident<128, 1, 1>(a, stream);
-  if (per_lane <= 2) return launch_resident<128, 2, 2>(a, stream);
-  if (per_lane <= 4) return launch_resident<128, 4, 4>(a, stream);
-  if (per_lane <= 7) return launch_resident<128, 7, 7>(a, stream);
-  if (per_lane <= 8) return launch_resident<128, 8, 8>(a, stream);
+  // Four pairs in the ring (two in flight ahead of pass 1) while two CTAs still
+  // fit an SM's shared memory; three for the widest rows.
+  if (per_lane <= 1) return launch_resident<128, 1, 1, 4>(a, stream);
+  if (per_lane <= 2) return launch_resident<128, 2, 2, 4>(a, stream);
+  if (per_lane <= 4) return launch_resident<128, 4, 4, 4>(a, stream);
+  if (per_lane <= 7) return launch_resident<128, 7, 7, 4>(a, stream);
+  if (per_lane <= 8) return launch_resident<128, 8, 8, 3>(a, stream);
   return launch_generic(a, stream);
 }
 
