@@ -19,9 +19,17 @@
 // binary32 spacing is 1, so the addition itself rounds t half-to-even, and
 // subtracting the constant again is exact.
 //
+// s = fl(g * sigma) depends on the bf16 gate alone, so -- as the pages' fused
+// SwiGLU producer does with its SiLU table (FastVideo API page,
+// swiglu_quantize) -- each CTA first tabulates s for every bf16 gate with
+// 2^-25 <= |g| <= 87 (8,030 values, 32 KB of shared memory), computed with the
+// arithmetic above.  A warp whose gates all lie in that range looks s up and
+// only forms y = bf16(fl(s * u)); other warps compute s directly.  Both give
+// the same bits.
+//
 // Work layout as in the standalone quantize: one warp per 512-column segment,
-// one 16-element block per lane, 256-bit loads of gate and up.  When every
-// gate of the warp's segment has |g| <= 87 (all data in practice), 2^k is a
+// one 16-element block per lane, 256-bit loads of gate and up.  In the direct
+// computation, when every gate of the warp's segment has |g| <= 87, 2^k is a
 // normal number for every element and the scaling is a single multiply by a
 // power of two built from k's bits; otherwise the warp scales with ldexpf,
 // which gives identical results wherever both apply.
@@ -46,6 +54,19 @@ constexpr float kP6 = 0x1.6c16c2p-10f;    // fl(1/6!)
 constexpr float kP7 = 0x1.a01a02p-13f;    // fl(1/7!)
 constexpr float kRound = 0x1.8p+23f;      // 1.5 * 2^23
 constexpr float kFastLimit = 87.0f;       // |z| <= 87: k in [-126, 127]
+
+// SiLU products s(g) = fl(g * sigma(g)) of the bf16 gates with magnitude bits in
+// [kTabLo, kTabHi] (2^-25 <= |g| <= 87), both signs, tabulated per CTA in shared
+// memory: entry sign * 4096 + (magnitude bits - kTabLo).
+constexpr uint32_t kTabLo = 0x3300u;  // bf16 bits of 2^-25
+constexpr uint32_t kTabHi = 0x42aeu;  // bf16 bits of 87
+constexpr int kTabHalf = 4096;
+
+__device__ __forceinline__ uint32_t absmin_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
@@ -114,14 +135,65 @@ __device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u,
   }
 }
 
+// Byte offsets in the table of the gates in the low and high halves of a bf16 pair
+// whose magnitudes lie in [kTabLo, kTabHi]: w - (kTabLo, kTabLo) leaves
+// sign * 0x8000 + (magnitude - kTabLo) in each half without a borrow.
+__device__ __forceinline__ void table_offsets(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t d = w - (kTabLo | (kTabLo << 16));
+  lo = ((d << 2) & 0x3ffcu) | ((d >> 1) & 0x4000u);
+  hi = ((d >> 14) & 0x3ffcu) | ((d >> 17) & 0x4000u);
+}
+
+__device__ __forceinline__ void swiglu_block_table(const Block16& g, const Block16& u, Block16& y,
+                                                   const char* table) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo, hi;
+    table_offsets(g.w[i], lo, hi);
+    const float2 sv = make_float2(*reinterpret_cast<const float*>(table + lo),
+                                  *reinterpret_cast<const float*>(table + hi));
+    y.w[i] = float2_to_bf16x2(mul2(sv, bf16x2_to_float2(u.w[i])));
+  }
+}
+
+// Every gate of the block has magnitude in [kTabLo, kTabHi].
+__device__ __forceinline__ bool in_table(const Block16& g) {
+  const uint32_t mx = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(g.w[0], g.w[1]), absmax_bf16x2(g.w[2], g.w[3])),
+                                    absmax_bf16x2(absmax_bf16x2(g.w[4], g.w[5]), absmax_bf16x2(g.w[6], g.w[7])));
+  const uint32_t mn = absmin_bf16x2(absmin_bf16x2(absmin_bf16x2(g.w[0], g.w[1]), absmin_bf16x2(g.w[2], g.w[3])),
+                                    absmin_bf16x2(absmin_bf16x2(g.w[4], g.w[5]), absmin_bf16x2(g.w[6], g.w[7])));
+  const uint32_t mx_lo = mx & 0x7fffu, mx_hi = (mx >> 16) & 0x7fffu;
+  const uint32_t mn_lo = mn & 0x7fffu, mn_hi = (mn >> 16) & 0x7fffu;
+  return max(mx_lo, mx_hi) <= kTabHi && min(mn_lo, mn_hi) >= kTabLo;
+}
+
+// Fill the table: entries i and i + kTabHalf hold the positive and negative gate
+// of magnitude bits kTabLo + i (computed as a pair, the FAST exponential: |g| <= 87).
+__device__ __forceinline__ void fill_silu_table(float* table) {
+  for (int i = threadIdx.x; i < kTabHalf; i += blockDim.x) {
+    const uint32_t mag = kTabLo + static_cast<uint32_t>(i);
+    if (mag > kTabHi) continue;
+    const uint32_t pair = mag | ((mag | 0x8000u) << 16);  // (+g, -g)
+    const float2 gv = bf16x2_to_float2(pair);
+    const float2 e = exp_neg2<true>(gv);
+    const float2 d = add2(splat(1.0f), e);
+    const float2 sv = mul2(gv, rcp_rn_ge1(d));
+    table[i] = sv.x;
+    table[i + kTabHalf] = sv.y;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
 swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
               int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   __shared__ float inv_table[128];
+  __shared__ __align__(16) float silu_table[2 * kTabHalf];
   const float gsf = *gsf_ptr;
   fill_inverse_scales(inv_table, gsf);
+  fill_silu_table(silu_table);
   __syncthreads();
+  const char* table = reinterpret_cast<const char*>(silu_table);
 
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
@@ -161,8 +233,9 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       const bool in_row = row[u] < rows;
       const bool in_cols = g < groups;
       Block16 y;
-      const bool fast = block_amax(gb[u]) <= kFastLimit;
-      if (__all_sync(0xffffffffu, fast)) {
+      if (__all_sync(0xffffffffu, in_table(gb[u]))) {
+        swiglu_block_table(gb[u], ub[u], y, table);
+      } else if (__all_sync(0xffffffffu, block_amax(gb[u]) <= kFastLimit)) {
         swiglu_block<true>(gb[u], ub[u], y);
       } else {
         swiglu_block<false>(gb[u], ub[u], y);

@@ -81,6 +81,29 @@ def test_every_bf16_gate(dev):
         check_full(codes, scales, gate.shape[0], cols, co, so, f"every gate, up={u}, gsf={gsf}")
 
 
+def test_table_window_every_gate_and_its_edges(dev):
+    """Every bf16 gate the per-CTA SiLU table holds (2^-25 <= |g| <= 87, both
+    signs) laid out so that whole warps take the table path, then the same rows
+    with one gate per warp just outside the window (2^-25 minus one bf16 step,
+    87 plus one step), which sends those warps to the direct computation."""
+    mags = np.arange(0x3300, 0x42AF, dtype=np.uint16)
+    gates = np.concatenate([mags, mags | np.uint16(0x8000)])
+    rows, cols = 12, 8192
+    gen = np.random.default_rng(7)
+    g_bits = gates[gen.permutation(rows * cols) % gates.size].reshape(rows, cols)
+    assert set(np.unique(g_bits)) == set(gates.tolist())
+    up = workloads.swiglu_inputs(dev, rows=rows, cols=cols, seed=21)[1]
+    for edge in (None, 0x32FF, 0x42AF, 0xC2AF, 0xB2FF):
+        gb = g_bits.copy()
+        if edge is not None:
+            gb[:, ::512] = edge  # one gate in every 512-column segment
+        gate = torch.from_numpy(gb.view(np.int16)).view(torch.bfloat16).to(dev)
+        gsf = _oracle_gsf(gate, up)
+        codes, scales = _run(dev, gate, up, gsf)
+        co, so, _ = oracle.swiglu_rows(bits(gate), bits(up), gsf, threads=THREADS)
+        check_full(codes, scales, rows, cols, co, so, f"swiglu table window edge={edge}")
+
+
 def test_packed_gate_up_projection_views(dev):
     """gate and up as the two halves of one [rows, 2F] projection (ld = 2F)."""
     rows, f = 200, 1536
