@@ -84,10 +84,18 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each kernel is compiled from (its own file and the shared device header).
+KERNEL_SOURCES = {
+    "adaln_kernel": ("adaln.cu", "h3q_device.cuh"),
+    "swiglu_kernel": ("swiglu.cu", "h3q_device.cuh"),
+    "quantize_kernel": ("quantize.cu", "h3q_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     csrc = os.path.join(ROOT, "nvfp4_activation_quantize_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -99,7 +107,7 @@ def recorded_traffic(kernel: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split()
