@@ -86,7 +86,7 @@ def hbm_peak():
 
 # The sources each kernel is compiled from (its own file and the shared device header).
 KERNEL_SOURCES = {
-    "adaln_kernel": ("adaln.cu", "h3q_device.cuh"),
+    "adaln_block_kernel": ("adaln.cu", "h3q_device.cuh"),
     "swiglu_kernel": ("swiglu.cu", "h3q_device.cuh"),
     "quantize_kernel": ("quantize.cu", "h3q_device.cuh"),
 }
@@ -320,10 +320,10 @@ def run_ours(args, rank, world, dev):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic("adaln_kernel"),
+            "traffic": recorded_traffic("adaln_block_kernel"),
             "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "kernel": "adaln_kernel<7>",
+            "kernel": "adaln_block_kernel<448, 7> (7,168 columns, one 448-thread CTA per SM)",
             "launch_ms": round(launch_ms, 5),
         },
         "gpu_launches": args.steps,

@@ -28,7 +28,9 @@
 // copy is issued two iterations before its pass 1.  Rows are processed in pairs,
 // which shares one barrier and the table registers between two independent
 // rows' arithmetic.
-// Rows wider than 8,192 take a generic kernel with the same chunk-to-thread
+// Rows of exactly 7,168 columns take a block-per-thread kernel (one CTA of
+// 448 threads per SM, described above it) with the same pass-1 order; rows
+// wider than 8,192 take a generic kernel with the same chunk-to-thread
 // mapping and order that reads x twice and the tables per row.
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
@@ -463,6 +465,243 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
   zero_padding_rows(a);
 }
 
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// bf16(v) as the fp32 value it stands for: cvt.rn.bf16x2 puts bf16(v) in the
+// upper half and bf16(0) = 0 in the lower, which is that value's fp32 pattern.
+__device__ __forceinline__ float bf16_round(float v) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(v), "f"(0.0f));
+  return __uint_as_float(r);
+}
+
+// Modulate and quantize one full 16-element block (x words v[k][0..7], chunks
+// 2b and 2b+1) of R rows, and store its 8 code bytes and scale byte per row.
+template <int R>
+__device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const float (&rstd)[R],
+                                           const ChunkTables (&tb)[2],
+                                           uint8_t* const (&codes_at)[R],
+                                           uint8_t* const (&scale_at)[R], float gsf,
+                                           const float* inv_table) {
+  float2 y[R][8];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const float2 rstd2 = make_float2(rstd[k], rstd[k]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const ChunkTables& t = tb[i >> 2];
+      const float2 n = mul2(bf16x2_to_float2(v[k][i]), rstd2);
+      const float2 h = mul2(n, t.gm[i & 3]);
+      const float2 m = mul2(h, t.fc[i & 3]);
+      const float2 o = add_bf16x2_f32(t.sh[i & 3], m);
+      y[k][i] = make_float2(bf16_round(o.x), bf16_round(o.y));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(y[k][i].x), fabsf(y[k][i].y)));
+    const uint32_t sf = block_scale(amax, gsf);
+    const float inv = inv_table[sf];
+    const float2 inv2 = make_float2(inv, inv);
+    const uint32_t lo = e2m1x8(mul2(y[k][0], inv2), mul2(y[k][1], inv2), mul2(y[k][2], inv2), mul2(y[k][3], inv2));
+    const uint32_t hi = e2m1x8(mul2(y[k][4], inv2), mul2(y[k][5], inv2), mul2(y[k][6], inv2), mul2(y[k][7], inv2));
+    store_codes(codes_at[k], lo, hi);
+    store_byte(scale_at[k], sf);
+  }
+}
+
+// Rows of exactly 16 * NB columns with NB = 448 (7,168, the attention width):
+// one CTA of NB threads per SM, thread t owning 16-element block t of every row
+// in pass 2, so a thread quantizes whole blocks (one scale computation per
+// block, no exchange between threads) and keeps the tables of only 16 columns
+// (40 registers).  Pass 1 keeps the canonical order: R = NB / 128 = 3 groups of
+// 128 lanes, group g summing row g of each 3-row step (chunk c on lane c % 128).
+// x streams through a ring of kStages steps of R rows, each pass-1 lane copying
+// its own chunks; chunk c sits at slot c ^ ((c >> 3) & 1), which keeps both the
+// pass-1 reads (lane l, chunk l + 128 j) and the pass-2 reads (thread t, chunks
+// 2t and 2t + 1) free of bank conflicts.  A step's rows are read by every thread
+// in pass 2 only after the barrier that follows their pass 1.  The first warp
+// outside the pass-1 groups publishes, per row of the step about to be emitted,
+// the rstd (from the warp totals, one lane per row), the frame and the row's
+// scale offset, and announces them on a named barrier that the other warps wait
+// on before pass 2; the per-row bookkeeping is thus done once per row, not once
+// per thread.
+// Per-row values published by the stats warp for one step.
+struct RowInfo {
+  float rstd;
+  int32_t frame;
+  int64_t scale_off;  // byte offset of the row's part of a scale word (scale_row_offset)
+};
+
+template <int NB, int C1>
+__global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
+  constexpr int R = NB / kLanes128;
+  constexpr int kStages = 4;
+  constexpr int kChunks = kLanes128 * C1;
+  constexpr int64_t kCodeRow = 8 * NB;  // code bytes per row (cols / 2)
+  static_assert(kChunks == 2 * NB, "one thread per 16-element block");
+  constexpr int kStatsWarp = R * kLanes128 / 32;
+  static_assert(kStatsWarp < NB / 32, "needs a warp outside the pass-1 groups");
+  extern __shared__ uint4 ring[];  // [kStages][R][kChunks]
+  __shared__ float inv_table[128];
+  __shared__ float totals[2][R][4];
+  __shared__ RowInfo rows_s[2][R];
+  const float gsf = *a.gsf;
+  fill_inverse_scales(inv_table, gsf);
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int lane = t & 31;
+  const int grp = t >> 7;
+  const int l = t & 127;
+  const bool p1 = grp < R;  // warp-uniform
+  const int64_t quads = a.cols >> 6;
+  const float cols_f = static_cast<float>(a.cols);
+  const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
+  const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
+  const int64_t steps = (r_end - r_begin + R - 1) / R;
+  const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+
+  // pass-1 lanes: the next row to copy and its ring slot
+  const uint16_t* x_next = a.x + (r_begin + grp) * a.ld + l * 8;
+  const int64_t x_step = R * a.ld;
+  const int l_slot = l ^ ((l >> 3) & 1);  // chunk c at slot c ^ ((c >> 3) & 1): conflict-free in both passes
+  const uint32_t ring_l = ring_base + static_cast<uint32_t>(grp * kChunks + l_slot) * 16;
+  int issued = 0;  // steps issued so far
+  auto issue = [&]() {
+    if (p1 && issued < steps && r_begin + R * issued + grp < r_end) {
+      const uint32_t dst = ring_l + static_cast<uint32_t>((issued % kStages) * R * kChunks) * 16;
+#pragma unroll
+      for (int j = 0; j < C1; ++j) cp_async16(dst + j * (kLanes128 * 16), x_next + j * (kLanes128 * 8));
+    }
+    cp_async_commit();
+    x_next += x_step;
+    ++issued;
+  };
+  auto pass1 = [&](int64_t q) {
+    if (q >= steps || !p1) return;
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    if (r_begin + R * q + grp < r_end) {
+      const uint4* buf = ring + ((q % kStages) * R + grp) * kChunks + l_slot;
+#pragma unroll
+      for (int j = 0; j < C1; ++j) accumulate(buf[j * kLanes128], acc);
+    }
+    float tot = __fadd_rn(__fadd_rn(__fadd_rn(acc[0].x, acc[0].y), __fadd_rn(acc[1].x, acc[1].y)),
+                          __fadd_rn(__fadd_rn(acc[2].x, acc[2].y), __fadd_rn(acc[3].x, acc[3].y)));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, o));
+    if (lane == 0) totals[q & 1][grp][warp & 3] = tot;
+  };
+  // the stats warp: lane k < R publishes row k of step q
+  FrameCursor lane_cursor(a, r_begin + (lane < R ? lane : 0));
+  auto stats = [&](int64_t q) {
+    if (q >= steps || lane >= R) return;
+    const int64_t r = r_begin + R * q + lane;
+    const float* T = totals[q & 1][lane];
+    RowInfo info;
+    info.rstd = rstd_of(__fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3])), cols_f, a.eps);
+    info.frame = r < r_end ? static_cast<int32_t>(lane_cursor.at(a, r)) : -1;
+    info.scale_off = scale_row_offset(r, quads);
+    rows_s[q & 1][lane] = info;
+    if (a.row_rstd != nullptr && r < r_end) a.row_rstd[r] = info.rstd;
+  };
+
+  ChunkTables tb[2];
+  int32_t frame = -1;
+  auto use_frame = [&](int32_t f) {  // CTA-uniform
+    if (f == frame) return;
+    frame = f;
+    load_tables(a, f, 2 * t, tb[0]);
+    load_tables(a, f, 2 * t + 1, tb[1]);
+  };
+
+#pragma unroll
+  for (int q = 0; q < kStages - 1; ++q) issue();
+  cp_async_wait<kStages - 2>();  // step 0 landed (this thread's copies)
+  pass1(0);
+  __syncthreads();  // inv_table, step 0's totals and copies
+
+  uint8_t* code_step = a.codes + r_begin * kCodeRow + t * 8;
+  uint8_t* const scale_t = a.scales + (t >> 2) * 512 + (t & 3);
+  for (int64_t q = 0; q < steps; ++q) {
+    if (warp == kStatsWarp) {
+      stats(q);
+      __syncwarp();
+      named_arrive(1, NB);
+    }
+    issue();
+    cp_async_wait<kStages - 2>();  // step q+1 landed (this thread's copies)
+    pass1(q + 1);
+    if (warp != kStatsWarp) named_sync(1, NB);  // rows of step q published
+
+    const int n = static_cast<int>(r_end - r_begin - R * q < R ? r_end - r_begin - R * q : R);
+    const uint4* buf = ring + (q % kStages) * R * kChunks + 2 * t;
+    const int sw = (t >> 2) & 1;
+    RowInfo info[R];
+    bool one_frame = n == R;  // all R rows present and in one frame (frames need not be monotone)
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      info[k] = rows_s[q & 1][k];
+      one_frame = one_frame && info[k].frame == info[0].frame;
+    }
+    if (one_frame) {
+      use_frame(info[0].frame);
+      uint32_t v[R][8];
+      float rs[R];
+      uint8_t* ca[R];
+      uint8_t* sa[R];
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        const uint4 lo = buf[k * kChunks + sw], hi = buf[k * kChunks + 1 - sw];
+        v[k][0] = lo.x; v[k][1] = lo.y; v[k][2] = lo.z; v[k][3] = lo.w;
+        v[k][4] = hi.x; v[k][5] = hi.y; v[k][6] = hi.z; v[k][7] = hi.w;
+        rs[k] = info[k].rstd;
+        ca[k] = code_step + k * kCodeRow;
+        sa[k] = scale_t + info[k].scale_off;
+      }
+      emit_block<R>(v, rs, tb, ca, sa, gsf, inv_table);
+    } else {
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        if (k >= n) break;  // CTA-uniform
+        use_frame(info[k].frame);
+        uint32_t v[1][8];
+        const uint4 lo = buf[k * kChunks + sw], hi = buf[k * kChunks + 1 - sw];
+        v[0][0] = lo.x; v[0][1] = lo.y; v[0][2] = lo.z; v[0][3] = lo.w;
+        v[0][4] = hi.x; v[0][5] = hi.y; v[0][6] = hi.z; v[0][7] = hi.w;
+        const float rs[1] = {info[k].rstd};
+        uint8_t* const ca[1] = {code_step + k * kCodeRow};
+        uint8_t* const sa[1] = {scale_t + info[k].scale_off};
+        emit_block<1>(v, rs, tb, ca, sa, gsf, inv_table);
+      }
+    }
+    code_step += R * kCodeRow;
+    __syncthreads();  // step q+1's totals and copies; step q's ring stage and rows are free
+  }
+  cp_async_wait<0>();
+  zero_padding_rows(a);
+}
+
+cudaError_t launch_block7168(const AdalnArgs& a, cudaStream_t stream) {
+  constexpr int NB = 448, C1 = 7, R = NB / kLanes128;
+  const int smem = 4 * R * kLanes128 * C1 * 16;
+  int blocks = 0;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1>), NB,
+                                      smem, a.rows > 0 ? (a.rows + R - 1) / R : 1, &blocks);
+  if (err != cudaSuccess) return err;
+  adaln_block_kernel<NB, C1><<<blocks, NB, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 template <int NT, int J, int C1, int S>
 cudaError_t launch_resident(const AdalnArgs& a, cudaStream_t stream) {
   const int smem = S * 2 * kLanes128 * C1 * 16;
@@ -504,6 +743,7 @@ cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
   if (per_lane <= 1) return launch_resident<128, 1, 1, 4>(a, stream);
   if (per_lane <= 2) return launch_resident<128, 2, 2, 4>(a, stream);
   if (per_lane <= 4) return launch_resident<128, 4, 4, 4>(a, stream);
+  if (chunks == 2 * 448) return launch_block7168(a, stream);  // 7,168 columns
   if (per_lane <= 7) return launch_resident<128, 7, 7, 4>(a, stream);
   if (per_lane <= 8) return launch_resident<128, 8, 8, 3>(a, stream);
   return launch_generic(a, stream);

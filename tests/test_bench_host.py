@@ -4,12 +4,12 @@ import bench
 
 
 def test_recorded_traffic_follows_the_source_hash(monkeypatch):
-    value = bench.recorded_traffic("adaln_kernel")
+    value = bench.recorded_traffic("adaln_block_kernel")
     assert value is not None and value > 0
     # ~ the algorithmic bytes of the 65,280 x 7,168 workload (reads once, writes partly in L2)
     assert 0.8 * bench.adaln_bytes(65280, 7168, 32) < value < 1.2 * bench.adaln_bytes(65280, 7168, 32)
     monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0" * 16)
-    assert bench.recorded_traffic("adaln_kernel") is None
+    assert bench.recorded_traffic("adaln_block_kernel") is None
     assert bench.recorded_traffic("no_such_kernel") is None
 
 

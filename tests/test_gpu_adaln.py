@@ -82,6 +82,47 @@ def test_row_frame_array_and_strided_x(dev):
     assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))
 
 
+@pytest.mark.parametrize("rows", [1, 2, 3, 4, 5, 7, 457, 1000])
+def test_7168_row_frame_array_strided_and_ragged_steps(dev, rows):
+    """The 7,168-column kernel (three rows per step, one block per thread) with a
+    per-row random frame (frames change inside every step), x as a strided view,
+    row counts that leave partial steps and CTAs with one or two rows, and the
+    per-row rstd output."""
+    cols, frames_n = 7168, 7
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols + 256, frames=frames_n, seed=rows + 70)
+    w["x"] = w["x"][:, 128:128 + cols]
+    w["gamma"] = w["gamma"][:cols].contiguous()
+    w["table"] = w["table"][:, :, :cols].contiguous()
+    gen = torch.Generator(device="cpu").manual_seed(rows)
+    rf = torch.randint(0, frames_n, (rows,), generator=gen, dtype=torch.int32)
+    gsf = _oracle_gsf(w, rf.numpy())
+    codes, scales, rstd = _run(dev, w, gsf, row_frame=rf.to(dev))
+    co, so, ro, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), rf.numpy(),
+                                      w["eps"], gsf, threads=THREADS)
+    check_full(codes, scales, rows, cols, co, so, f"adaln 7168 row_frame {rows}")
+    check_padding(scales, rows, cols, f"adaln 7168 row_frame {rows}")
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))
+
+
+def test_7168_zero_rows_and_eps(dev):
+    """All-zero and constant rows at 7,168 columns, eps 0 and 0.5."""
+    rows, cols = 96, 7168
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=2, rows_per_frame=48, seed=31)
+    w["x"][5:9] = 0
+    w["x"][20:23] = -2.5
+    for eps in (0.5, 0.0):
+        if eps == 0.0:
+            w["x"][5:9] = 0.125  # keep rstd finite
+        w["eps"] = eps
+        frames = np.arange(rows) // 48
+        gsf = _oracle_gsf(w, frames)
+        codes, scales, rstd = _run(dev, w, gsf, rows_per_frame=48)
+        co, so, ro, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames,
+                                          eps, gsf, threads=THREADS)
+        check_full(codes, scales, rows, cols, co, so, f"adaln 7168 eps={eps}")
+        assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))
+
+
 def test_eps_and_constant_rows(dev):
     """All-zero rows (rstd = 1/sqrt(eps)), constant rows and a large eps."""
     rows, cols = 64, 512
