@@ -67,6 +67,8 @@ _SIGNATURES = {
     "orc_swiglu_value": ([_F, _F], _F),
     "orc_quantize_block": ([_P, _F, _P, _P], None),
     "orc_global_scale": ([_F], _F),
+    "orc_amax_bf16": ([_P, _I64], _F),
+    "orc_global_scale_from_amax": ([_F], _F),
     "orc_scale_offset": ([_I64, _I64, _I64], _I64),
     "orc_padded_rows": ([_I64], _I64),
     "orc_scale_offsets_rows": ([_P, _I64, _I64, _P], None),
@@ -199,6 +201,17 @@ def global_scale(amax: float) -> float:
     if not amax > 0:
         raise ValueError("global amax must be positive")
     return float(lib().orc_global_scale(float(amax)))
+
+
+def amax_bf16(bits: np.ndarray) -> float:
+    """max |v| over bf16 values given as uint16 bit patterns (exact; 0 when empty)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    return float(lib().orc_amax_bf16(_ptr(b), b.size))
+
+
+def global_scale_from_amax(amax: float) -> float:
+    """fl(2688 / amax) with amax = 0 giving 1 and +inf clamped to the largest float."""
+    return float(lib().orc_global_scale_from_amax(float(amax)))
 
 
 # --------------------------------------------------------------------------- #

@@ -27,11 +27,15 @@
  *             SiLU-and-mul producer, attention-output quantize).
  *   [FV-LOG]  FastVideo commit log, branch vae-parallel-decode: the modulation
  *             index contract [0, table_rows) and the int64 indexing fix.
+ *   [FV-API], NVFP4DecoderLinear; [FlashRT] FlashRT PR #142 "FP8/NVFP4
+ *             kernelized inference pipeline", commit "...amax pipeline": the
+ *             dynamic (per-call abs-max) and calibrated (running-max) scales.
  *
  * Readings where the pages are silent or use approximate arithmetic are
  * stated next to each function (division and reciprocal are correctly
  * rounded; the SiLU exponential is the fixed operation sequence exp_c).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -270,6 +274,35 @@ void orc_quantize_block(const float y[16], float gsf, uint8_t *sf_out, uint8_t p
  * largest E4M3 scale (448) with its largest element on the largest E2M1
  * magnitude (6): gsf = fl(448 * 6 / amax). */
 float orc_global_scale(float amax) { return 2688.0f / amax; }
+
+/* Dynamic and calibrated scales (f3).  [FV-API] NVFP4DecoderLinear: a dynamic
+ * layer scales each call by the abs-max of its input; a calibrating layer folds
+ * each call's abs-max into a persistent running maximum (input_amax).
+ * [FlashRT] commit "...amax pipeline": the abs-max is taken on the device in a
+ * pass of its own and read by the quantize pass, with no host synchronisation.
+ *
+ * orc_amax_bf16: max |v| over n bf16 values (exact; 0 for n = 0; NaN is outside
+ * the contract).  orc_global_scale_from_amax: the global scale of an abs-max,
+ * with two readings where the formula has no finite positive value: amax = 0
+ * (an all-zero tensor, whose codes and scales are zero under any scale) gives 1,
+ * and amax = +inf (a producer output that overflowed bf16) is clamped to the
+ * largest finite binary32 first. */
+float orc_amax_bf16(const uint16_t *v, int64_t n)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(orc_bf16_value(v[i]));
+        if (a > m) m = a;
+    }
+    return m;
+}
+
+float orc_global_scale_from_amax(float amax)
+{
+    if (amax == 0.0f) return 1.0f;
+    if (amax > FLT_MAX) amax = FLT_MAX;
+    return 2688.0f / amax;
+}
 
 /* ------------------------------------------------------------------------ */
 /* 128x4 scale layout                                                         */
