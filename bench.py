@@ -101,10 +101,10 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def recorded_traffic(kernel: str, path: str | None = None):
     """DRAM bytes per launch of `kernel` from profiles/dram_traffic.txt, if they were
     taken from the current kernel sources (lines: kernel source-hash bytes note)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    path = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     want = kernel_source_hash(kernel)
@@ -419,6 +419,32 @@ def measure_producers(h3q, dev, stream, args):
         _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream)
         res[f"attn_out_quantize_{tokens}x7168"] = entry(quantize_bytes(*x.shape), per, tokens)
         del x, c, s
+
+    # dynamic AdaLN: per-call abs-max pass, device global scale, producer (three
+    # launches and an fp32 zero fill per step, no host synchronisation); GB/s by the
+    # single-pass algorithmic bytes, although x is read twice
+    w = workloads.adaln_inputs(dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    c = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
+
+    def dynamic_step():
+        amax.zero_()
+        h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], rows_per_frame=RPF, eps=w["eps"],
+                                   amax=amax, stream=stream)
+        h3q.h3q_global_scale_from_amax(amax, g, stream=stream)
+        h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], g, rows_per_frame=RPF,
+                                    eps=w["eps"], codes=c, scales=s, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dynamic_step()
+    _, per = time_launches(dynamic_step, n, stream)
+    res["adaln_dynamic_scale_65280x7168"] = entry(adaln_bytes(ROWS, COLS, FRAMES), per, ROWS)
+    res["adaln_dynamic_scale_65280x7168"]["note"] = ("abs-max pass + device scale + producer; x is read "
+                                                     "twice, GB/s by the single-pass bytes")
+    del w, c, s
 
     # standalone quantize 8,192 x 7,168 (150 MB: near L2, so L2 is flushed before each launch)
     x = workloads.quantize_inputs(dev)

@@ -173,6 +173,46 @@ int h3q_swiglu_nvfp4(const void *gate, int64_t ld_gate, const void *up, int64_t 
 int h3q_dequantize_nvfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t cols,
                          const float *global_scale, float *out, void *stream);
 
+/*
+ * Dynamic and calibrated global scales.
+ *
+ * FastVideo API page, NVFP4DecoderLinear: a dynamic layer scales each call by
+ * the abs-max of its input, and a calibrating layer folds each call's abs-max
+ * into a persistent running maximum (input_amax).  FlashRT PR #142, commit
+ * "...amax pipeline": the abs-max is taken on the device in a pass of its own
+ * and read by the quantize pass with no host synchronisation.
+ *
+ * The three abs-max passes compute the producer's bf16 output y exactly as the
+ * producer does (same arguments, same arithmetic) without storing it, and fold
+ * max |y| into *amax: *amax = max(*amax, max |y|).  Zero *amax first for a
+ * per-call abs-max; keep it across calls for a running maximum.
+ *
+ *   amax  device fp32 scalar, 4-byte aligned, holding a value >= 0 (+0.0, not
+ *         -0.0) on entry; updated with an atomic maximum, so several passes
+ *         may fold into it, on one stream or several.
+ *
+ * Then h3q_global_scale_from_amax writes *global_scale = fl(2688 / *amax) on the
+ * device (2688 = 448 * 6), with two readings where that has no finite positive
+ * value: amax = 0 gives 1, and +inf (a producer output that overflowed bf16) is
+ * clamped to the largest finite binary32 first.  The producer then reads it.
+ * Nothing synchronises; the calls are ordered by the stream.
+ *
+ * Preconditions and status codes are those of the matching producer (shapes,
+ * alignment, ld, frames), plus: amax not NULL and not overlapping an input.
+ */
+int h3q_amax_bf16(const void *x, int64_t ld_x, int64_t rows, int64_t cols, float *amax,
+                  void *stream);
+
+int h3q_rmsnorm_adaln_amax(const void *x, int64_t ld_x, const void *gamma,
+                           const void *mod_table, int64_t num_frames, const int32_t *row_frame,
+                           int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
+                           float *amax, void *stream);
+
+int h3q_swiglu_amax(const void *gate, int64_t ld_gate, const void *up, int64_t ld_up,
+                    int64_t rows, int64_t cols, float *amax, void *stream);
+
+int h3q_global_scale_from_amax(const float *amax, float *global_scale, void *stream);
+
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char *h3q_last_error(void);
 

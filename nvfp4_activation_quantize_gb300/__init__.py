@@ -22,6 +22,7 @@ __all__ = [
     "H3Q_OK", "H3Q_ERR_INVALID_ARGUMENT", "H3Q_ERR_CUDA", "H3QError", "library", "library_path",
     "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
+    "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
 ]
 
 H3Q_OK = 0
@@ -36,6 +37,10 @@ _SIGNATURES = {
                                 _P, _P, _P, _P, _P],
     "h3q_swiglu_nvfp4": [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "h3q_dequantize_nvfp4": [_P, _P, _I64, _I64, _P, _P, _P],
+    "h3q_amax_bf16": [_P, _I64, _I64, _I64, _P, _P],
+    "h3q_rmsnorm_adaln_amax": [_P, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _I64, _I64, _P, _P],
+    "h3q_swiglu_amax": [_P, _I64, _P, _I64, _I64, _I64, _P, _P],
+    "h3q_global_scale_from_amax": [_P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -251,3 +256,94 @@ def h3q_dequantize_nvfp4(codes, scales, global_scale, out=None, stream=None):
                                             gsf.data_ptr(), out.data_ptr(), _stream(stream, dev))
     _check("h3q_dequantize_nvfp4", rc)
     return out
+
+
+# --------------------------------------------------------------------------- #
+# dynamic and calibrated global scales                                          #
+# --------------------------------------------------------------------------- #
+
+def _amax_buffer(amax, device):
+    import torch
+
+    if amax is None:
+        amax = torch.zeros(1, dtype=torch.float32, device=device)
+    _cuda_tensor("amax", amax, torch.float32, device)
+    if amax.numel() != 1:
+        raise ValueError("amax must hold one fp32 value")
+    return amax
+
+
+def h3q_amax_bf16(x, amax=None, stream=None):
+    """Fold max |x| of bf16 x [rows, cols] into the fp32 device scalar ``amax``
+    (a new zero scalar when None); returns amax."""
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    amax = _amax_buffer(amax, x.device)
+    with torch.cuda.device(x.device):
+        rc = library().h3q_amax_bf16(x.data_ptr(), ld, rows, cols, amax.data_ptr(),
+                                     _stream(stream, x.device))
+    _check("h3q_amax_bf16", rc)
+    return amax
+
+
+def h3q_rmsnorm_adaln_amax(x, gamma, mod_table, *, row_frame=None, rows_per_frame=None, eps=1e-6,
+                           amax=None, stream=None):
+    """Fold max |y| of the RMSNorm + AdaLN output y (the bf16 values the producer
+    quantizes, same arguments) into ``amax``; returns amax."""
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    dev = x.device
+    _contiguous("gamma", gamma, torch.bfloat16, (cols,), dev)
+    _cuda_tensor("mod_table", mod_table, torch.bfloat16, dev)
+    if mod_table.dim() != 3 or mod_table.shape[1:] != (2, cols) or not mod_table.is_contiguous():
+        raise ValueError("mod_table must be contiguous [frames, 2, cols]")
+    rf_ptr = None
+    if row_frame is not None:
+        _contiguous("row_frame", row_frame, torch.int32, (rows,), dev)
+        rf_ptr = row_frame.data_ptr()
+        rows_per_frame = 0
+    elif rows_per_frame is None:
+        raise ValueError("give row_frame or rows_per_frame")
+    amax = _amax_buffer(amax, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_rmsnorm_adaln_amax(
+            x.data_ptr(), ld, gamma.data_ptr(), mod_table.data_ptr(), mod_table.shape[0], rf_ptr,
+            int(rows_per_frame), float(eps), rows, cols, amax.data_ptr(), _stream(stream, dev))
+    _check("h3q_rmsnorm_adaln_amax", rc)
+    return amax
+
+
+def h3q_swiglu_amax(gate, up, amax=None, stream=None):
+    """Fold max |bf16(silu(gate) * up)| into ``amax``; returns amax."""
+    import torch
+
+    gate, rows, cols, ldg = _rows_view("gate", gate, torch.bfloat16)
+    dev = gate.device
+    up, rows_u, cols_u, ldu = _rows_view("up", up, torch.bfloat16, dev)
+    if (rows_u, cols_u) != (rows, cols):
+        raise ValueError("gate and up must have the same shape")
+    amax = _amax_buffer(amax, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_swiglu_amax(gate.data_ptr(), ldg, up.data_ptr(), ldu, rows, cols,
+                                       amax.data_ptr(), _stream(stream, dev))
+    _check("h3q_swiglu_amax", rc)
+    return amax
+
+
+def h3q_global_scale_from_amax(amax, global_scale=None, stream=None):
+    """The global scale fl(2688 / amax) computed on the device from the fp32 scalar
+    ``amax`` (0 gives 1; +inf is clamped); returns the fp32 scalar written."""
+    import torch
+
+    _cuda_tensor("amax", amax, torch.float32)
+    dev = amax.device
+    if global_scale is None:
+        global_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_global_scale_from_amax(amax.data_ptr(), global_scale.data_ptr(),
+                                                  _stream(stream, dev))
+    _check("h3q_global_scale_from_amax", rc)
+    return global_scale

@@ -56,6 +56,7 @@ struct AdalnArgs {
   uint8_t* codes;
   uint8_t* scales;
   float* row_rstd;
+  float* amax;  // abs-max pass: fold max |y| into *amax instead of quantizing (codes, scales unused)
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
@@ -205,13 +206,14 @@ __device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
 // chunk's tables, quantize this thread's half block of each row, store its four
 // code bytes at codes_at[k] and, from the even thread of the pair, the block's
 // scale byte at scale_at[k].  All 32 lanes of the warp call this (it
-// shuffles); `valid` masks the stores.
-template <int R>
+// shuffles); `valid` masks the stores.  With AMAX the chunk's max |y| is
+// folded into run_max instead (for valid chunks) and nothing is stored.
+template <int R, bool AMAX>
 __device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rstd)[R],
                                            const ChunkTables& tb, bool valid,
                                            uint8_t* const (&codes_at)[R],
                                            uint8_t* const (&scale_at)[R], float gsf,
-                                           const float* inv_table) {
+                                           const float* inv_table, float& run_max) {
   const int lane = threadIdx.x & 31;
   // Stages run across all R rows before the next stage, so that the rows'
   // independent work sits side by side for the scheduler.
@@ -233,6 +235,12 @@ __device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rs
   for (int k = 0; k < R; ++k)
     amax[k] = halves_amax(absmax_bf16x2(absmax_bf16x2(y[k][0], y[k][1]),
                                         absmax_bf16x2(y[k][2], y[k][3])));
+  if (AMAX) {
+#pragma unroll
+    for (int k = 0; k < R; ++k)
+      if (valid) run_max = fmaxf(run_max, amax[k]);
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < R; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], 1));
 #pragma unroll
@@ -268,14 +276,15 @@ __device__ __forceinline__ void zero_padding_rows(const AdalnArgs& a) {
 // pair p+1 and modulates and quantizes pair p, then one barrier publishes
 // pair p+1's warp totals.  Pass 2 of pair p reads chunks copied by other
 // threads; every thread's wait for pair p came before the previous barrier.
-template <int NT, int J, int C1, int S, bool FULL>
+template <int NT, int J, int C1, int S, bool FULL, bool AMAX>
 __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
   constexpr int kRow = kLanes128 * C1;  // chunk slots per row in the ring
   extern __shared__ uint4 ring[];
   __shared__ float inv_table[128];
   __shared__ float totals[2][2][4];
-  const float gsf = *a.gsf;
-  fill_inverse_scales(inv_table, gsf);
+  const float gsf = AMAX ? 0.0f : *a.gsf;
+  if (!AMAX) fill_inverse_scales(inv_table, gsf);
+  float run_max = 0.0f;
 
   const int t = threadIdx.x;
   const bool lane1 = t < kLanes128;  // a pass-1 lane (warp-uniform)
@@ -390,7 +399,7 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
         const uint4 v[2] = {buf[j * NT], buf[kRow + j * NT]};
         uint8_t* const ca[2] = {code_base[0] + j * (NT * 4), code_base[1] + j * (NT * 4)};
         uint8_t* const sa[2] = {scale_base[0] + j * (NT / 8 * 512), scale_base[1] + j * (NT / 8 * 512)};
-        emit_chunk<2>(v, rstd, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table);
+        emit_chunk<2, AMAX>(v, rstd, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table, run_max);
       }
     } else {
 #pragma unroll
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
           const float rs[1] = {rstd[k]};
           uint8_t* const ca[1] = {code_base[k] + j * (NT * 4)};
           uint8_t* const sa[1] = {scale_base[k] + j * (NT / 8 * 512)};
-          emit_chunk<1>(v, rs, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table);
+          emit_chunk<1, AMAX>(v, rs, tb[j], FULL || t + j * NT < chunks, ca, sa, gsf, inv_table, run_max);
         }
       }
     }
@@ -413,17 +422,22 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
     stage = next;
   }
   cp_async_wait<0>();
-  zero_padding_rows(a);
+  if (AMAX)
+    commit_amax(run_max, a.amax, inv_table);  // inv_table is unused in this mode
+  else
+    zero_padding_rows(a);
 }
 
 // Any width: the same chunk-to-thread mapping and order, x read from global
 // memory in both passes (the second read mostly hits L2) and the tables read
 // per chunk and row.
+template <bool AMAX>
 __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs a) {
   __shared__ float inv_table[128];
   __shared__ float totals[2][1][4];
-  const float gsf = *a.gsf;
-  fill_inverse_scales(inv_table, gsf);
+  const float gsf = AMAX ? 0.0f : *a.gsf;
+  if (!AMAX) fill_inverse_scales(inv_table, gsf);
+  float run_max = 0.0f;
   __syncthreads();
 
   const int t = threadIdx.x;
@@ -459,10 +473,13 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
       }
       uint8_t* const ca[1] = {a.codes + r * (a.cols >> 1) + c * 4};
       uint8_t* const sa[1] = {a.scales + scale_row_offset(r, quads) + (c >> 3) * 512 + ((c >> 1) & 3)};
-      emit_chunk<1>(v, rstd, tb, valid, ca, sa, gsf, inv_table);
+      emit_chunk<1, AMAX>(v, rstd, tb, valid, ca, sa, gsf, inv_table, run_max);
     }
   }
-  zero_padding_rows(a);
+  if (AMAX)
+    commit_amax(run_max, a.amax, inv_table);
+  else
+    zero_padding_rows(a);
 }
 
 __device__ __forceinline__ void named_arrive(int id, int count) {
@@ -481,13 +498,14 @@ __device__ __forceinline__ float bf16_round(float v) {
 }
 
 // Modulate and quantize one full 16-element block (x words v[k][0..7], chunks
-// 2b and 2b+1) of R rows, and store its 8 code bytes and scale byte per row.
-template <int R>
+// 2b and 2b+1) of R rows, and store its 8 code bytes and scale byte per row
+// (with AMAX: fold the block's max |y| into run_max instead).
+template <int R, bool AMAX>
 __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const float (&rstd)[R],
                                            const ChunkTables (&tb)[2],
                                            uint8_t* const (&codes_at)[R],
                                            uint8_t* const (&scale_at)[R], float gsf,
-                                           const float* inv_table) {
+                                           const float* inv_table, float& run_max) {
   float2 y[R][8];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
@@ -507,6 +525,10 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(y[k][i].x), fabsf(y[k][i].y)));
+    if (AMAX) {  // abs-max pass: no quantize, no store
+      run_max = fmaxf(run_max, amax);
+      continue;
+    }
     const uint32_t sf = block_scale(amax, gsf);
     const float inv = inv_table[sf];
     const float2 inv2 = make_float2(inv, inv);
@@ -540,7 +562,7 @@ struct RowInfo {
   int64_t scale_off;  // byte offset of the row's part of a scale word (scale_row_offset)
 };
 
-template <int NB, int C1>
+template <int NB, int C1, bool AMAX>
 __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   constexpr int R = NB / kLanes128;
   constexpr int kStages = 4;
@@ -553,8 +575,9 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   __shared__ float inv_table[128];
   __shared__ float totals[2][R][4];
   __shared__ RowInfo rows_s[2][R];
-  const float gsf = *a.gsf;
-  fill_inverse_scales(inv_table, gsf);
+  const float gsf = AMAX ? 0.0f : *a.gsf;
+  if (!AMAX) fill_inverse_scales(inv_table, gsf);
+  float run_max = 0.0f;
 
   const int t = threadIdx.x;
   const int warp = t >> 5;
@@ -668,7 +691,7 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
         ca[k] = code_step + k * kCodeRow;
         sa[k] = scale_t + info[k].scale_off;
       }
-      emit_block<R>(v, rs, tb, ca, sa, gsf, inv_table);
+      emit_block<R, AMAX>(v, rs, tb, ca, sa, gsf, inv_table, run_max);
     } else {
 #pragma unroll
       for (int k = 0; k < R; ++k) {
@@ -681,50 +704,70 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
         const float rs[1] = {info[k].rstd};
         uint8_t* const ca[1] = {code_step + k * kCodeRow};
         uint8_t* const sa[1] = {scale_t + info[k].scale_off};
-        emit_block<1>(v, rs, tb, ca, sa, gsf, inv_table);
+        emit_block<1, AMAX>(v, rs, tb, ca, sa, gsf, inv_table, run_max);
       }
     }
     code_step += R * kCodeRow;
     __syncthreads();  // step q+1's totals and copies; step q's ring stage and rows are free
   }
   cp_async_wait<0>();
-  zero_padding_rows(a);
+  if (AMAX)
+    commit_amax(run_max, a.amax, inv_table);  // inv_table is unused in this mode
+  else
+    zero_padding_rows(a);
 }
 
+template <bool AMAX>
 cudaError_t launch_block7168(const AdalnArgs& a, cudaStream_t stream) {
   constexpr int NB = 448, C1 = 7, R = NB / kLanes128;
   const int smem = 4 * R * kLanes128 * C1 * 16;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1>), NB,
-                                      smem, a.rows > 0 ? (a.rows + R - 1) / R : 1, &blocks);
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1, AMAX>),
+                                      NB, smem, a.rows > 0 ? (a.rows + R - 1) / R : 1, &blocks);
   if (err != cudaSuccess) return err;
-  adaln_block_kernel<NB, C1><<<blocks, NB, smem, stream>>>(a);
+  adaln_block_kernel<NB, C1, AMAX><<<blocks, NB, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <int NT, int J, int C1, int S>
+template <int NT, int J, int C1, int S, bool AMAX>
 cudaError_t launch_resident(const AdalnArgs& a, cudaStream_t stream) {
   const int smem = S * 2 * kLanes128 * C1 * 16;
   const bool full = a.cols / 8 == int64_t(NT) * J && a.cols / 8 == int64_t(kLanes128) * C1;
-  const void* kernel = full ? reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, true>)
-                            : reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, false>);
+  const void* kernel = full ? reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, true, AMAX>)
+                            : reinterpret_cast<const void*>(&adaln_kernel<NT, J, C1, S, false, AMAX>);
   int blocks = 0;
   cudaError_t err = persistent_blocks(kernel, NT, smem, a.rows > 0 ? a.rows : 1, &blocks);
   if (err != cudaSuccess) return err;
   if (full)
-    adaln_kernel<NT, J, C1, S, true><<<blocks, NT, smem, stream>>>(a);
+    adaln_kernel<NT, J, C1, S, true, AMAX><<<blocks, NT, smem, stream>>>(a);
   else
-    adaln_kernel<NT, J, C1, S, false><<<blocks, NT, smem, stream>>>(a);
+    adaln_kernel<NT, J, C1, S, false, AMAX><<<blocks, NT, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
+template <bool AMAX>
 cudaError_t launch_generic(const AdalnArgs& a, cudaStream_t stream) {
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_generic_kernel),
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_generic_kernel<AMAX>),
                                       kThreads, 0, a.rows > 0 ? a.rows : 1, &blocks);
   if (err != cudaSuccess) return err;
-  adaln_generic_kernel<<<blocks, kThreads, 0, stream>>>(a);
+  adaln_generic_kernel<AMAX><<<blocks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <bool AMAX>
+cudaError_t dispatch(const AdalnArgs& a, cudaStream_t stream) {
+  const int64_t chunks = a.cols / 8;
+  const int64_t per_lane = (chunks + kLanes128 - 1) / kLanes128;
+  // Four pairs in the ring (two in flight ahead of pass 1) while two CTAs still
+  // fit an SM's shared memory; three for the widest rows.
+  if (per_lane <= 1) return launch_resident<128, 1, 1, 4, AMAX>(a, stream);
+  if (per_lane <= 2) return launch_resident<128, 2, 2, 4, AMAX>(a, stream);
+  if (per_lane <= 4) return launch_resident<128, 4, 4, 4, AMAX>(a, stream);
+  if (chunks == 2 * 448) return launch_block7168<AMAX>(a, stream);  // 7,168 columns
+  if (per_lane <= 7) return launch_resident<128, 7, 7, 4, AMAX>(a, stream);
+  if (per_lane <= 8) return launch_resident<128, 8, 8, 3, AMAX>(a, stream);
+  return launch_generic<AMAX>(a, stream);
 }
 
 }  // namespace
@@ -734,19 +777,18 @@ cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                          int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
                          const float* gsf, uint8_t* codes, uint8_t* scales, float* row_rstd,
                          cudaStream_t stream) {
-  const AdalnArgs a{x,    ld,   gamma, table, num_frames, row_frame, rows_per_frame,
-                    eps,  rows, cols,  gsf,   codes,      scales,    row_rstd};
-  const int64_t chunks = cols / 8;
-  const int64_t per_lane = (chunks + kLanes128 - 1) / kLanes128;
-  // Four pairs in the ring (two in flight ahead of pass 1) while two CTAs still
-  // fit an SM's shared memory; three for the widest rows.
-  if (per_lane <= 1) return launch_resident<128, 1, 1, 4>(a, stream);
-  if (per_lane <= 2) return launch_resident<128, 2, 2, 4>(a, stream);
-  if (per_lane <= 4) return launch_resident<128, 4, 4, 4>(a, stream);
-  if (chunks == 2 * 448) return launch_block7168(a, stream);  // 7,168 columns
-  if (per_lane <= 7) return launch_resident<128, 7, 7, 4>(a, stream);
-  if (per_lane <= 8) return launch_resident<128, 8, 8, 3>(a, stream);
-  return launch_generic(a, stream);
+  const AdalnArgs a{x,    ld,   gamma, table,  num_frames, row_frame, rows_per_frame, eps,
+                    rows, cols, gsf,   codes,  scales,     row_rstd,  nullptr};
+  return dispatch<false>(a, stream);
+}
+
+cudaError_t launch_adaln_amax(const uint16_t* x, int64_t ld, const uint16_t* gamma,
+                              const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
+                              int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
+                              float* amax, cudaStream_t stream) {
+  const AdalnArgs a{x,    ld,   gamma,   table,   num_frames, row_frame, rows_per_frame, eps,
+                    rows, cols, nullptr, nullptr, nullptr,    nullptr,   amax};
+  return dispatch<true>(a, stream);
 }
 
 }  // namespace h3q

@@ -229,6 +229,91 @@ int h3q_swiglu_nvfp4(const void* gate, int64_t ld_gate, const void* up, int64_t 
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+// --- dynamic and calibrated scales ------------------------------------------
+
+namespace {
+int check_amax(const char* fn, const float* amax) {
+  if (amax == nullptr || !aligned(amax, 4)) return invalid(fn, "amax must be a 4-byte aligned pointer");
+  return 0;
+}
+}  // namespace
+
+int h3q_amax_bf16(const void* x, int64_t ld_x, int64_t rows, int64_t cols, float* amax,
+                  void* stream) {
+  static const char* fn = "h3q_amax_bf16";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_amax(fn, amax)) return e;
+  if (overlap(span(x, view_bytes(rows, cols, ld_x)), span(amax, 4))) return invalid(fn, "amax overlaps x");
+  cudaError_t err = h3q::launch_amax_bf16(static_cast<const uint16_t*>(x), ld_x, rows, cols, amax,
+                                          static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_rmsnorm_adaln_amax(const void* x, int64_t ld_x, const void* gamma, const void* mod_table,
+                           int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
+                           float eps, int64_t rows, int64_t cols, float* amax, void* stream) {
+  static const char* fn = "h3q_rmsnorm_adaln_amax";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
+  if (num_frames < 1) return invalid(fn, "num_frames must be >= 1");
+  if (num_frames > (int64_t(1) << 31)) return invalid(fn, "num_frames exceeds 2^31");
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_input(fn, "gamma", gamma, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "mod_table", mod_table, cols, 2 * num_frames, cols)) return e;
+  if (int e = check_amax(fn, amax)) return e;
+  if (row_frame != nullptr) {
+    if (!aligned(row_frame, 4)) return invalid(fn, "row_frame must be 4-byte aligned");
+  } else {
+    if (rows_per_frame < 1) return invalid(fn, "rows_per_frame must be >= 1 when row_frame is NULL");
+    if ((rows - 1) / rows_per_frame >= num_frames)
+      return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
+  }
+  const Span am = span(amax, 4);
+  if (overlap(am, span(x, view_bytes(rows, cols, ld_x))) || overlap(am, span(gamma, cols * 2)) ||
+      overlap(am, span(mod_table, num_frames * 4 * cols)) ||
+      (row_frame != nullptr && overlap(am, span(row_frame, rows * 4))))
+    return invalid(fn, "amax overlaps an input");
+  cudaError_t err = h3q::launch_adaln_amax(
+      static_cast<const uint16_t*>(x), ld_x, static_cast<const uint16_t*>(gamma),
+      static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, eps, rows,
+      cols, amax, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_swiglu_amax(const void* gate, int64_t ld_gate, const void* up, int64_t ld_up,
+                    int64_t rows, int64_t cols, float* amax, void* stream) {
+  static const char* fn = "h3q_swiglu_amax";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "gate", gate, ld_gate, rows, cols)) return e;
+  if (int e = check_input(fn, "up", up, ld_up, rows, cols)) return e;
+  if (int e = check_amax(fn, amax)) return e;
+  const Span am = span(amax, 4);
+  if (overlap(am, span(gate, view_bytes(rows, cols, ld_gate))) ||
+      overlap(am, span(up, view_bytes(rows, cols, ld_up))))
+    return invalid(fn, "amax overlaps an input");
+  cudaError_t err = h3q::launch_swiglu_amax(static_cast<const uint16_t*>(gate), ld_gate,
+                                            static_cast<const uint16_t*>(up), ld_up, rows, cols,
+                                            amax, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_global_scale_from_amax(const float* amax, float* global_scale, void* stream) {
+  static const char* fn = "h3q_global_scale_from_amax";
+  g_last_error.clear();
+  if (int e = check_amax(fn, amax)) return e;
+  if (global_scale == nullptr || !aligned(global_scale, 4))
+    return invalid(fn, "global_scale must be a 4-byte aligned pointer");
+  cudaError_t err = h3q::launch_global_scale(amax, global_scale, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
                          const float* global_scale, float* out, void* stream) {
   static const char* fn = "h3q_dequantize_nvfp4";

@@ -250,6 +250,31 @@ __device__ __forceinline__ Quantized quantize_block(const Block16& y, float gsf,
 }
 
 // ---------------------------------------------------------------------------
+// Abs-max accumulation (dynamic and calibrated scales)
+// ---------------------------------------------------------------------------
+
+// Fold each thread's running maximum m >= 0 into *amax: a warp maximum, a CTA
+// maximum through shared memory, one atomicMax per CTA on the binary32 bits
+// (for values >= 0 -- +inf included -- the bit patterns order as the values
+// do, so an integer maximum is the float maximum).  Every thread of the CTA
+// calls this once, after its last use of the shared scratch it is given
+// (32 floats).
+__device__ __forceinline__ void commit_amax(float m, float* amax, float* scratch32) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) scratch32[warp] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int nwarps = (blockDim.x + 31) >> 5;
+    float v = static_cast<int>(threadIdx.x) < nwarps ? scratch32[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(v));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 128x4 scale layout
 // ---------------------------------------------------------------------------
 

@@ -27,6 +27,20 @@ cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t*
                           int64_t ld_up, int64_t rows, int64_t cols, const float* gsf,
                           uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
+// Abs-max passes (dynamic and calibrated scales): fold max |y| of the producer's
+// bf16 output y into *amax (which must hold a value >= 0) without storing y.
+cudaError_t launch_amax_bf16(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
+                             float* amax, cudaStream_t stream);
+cudaError_t launch_adaln_amax(const uint16_t* x, int64_t ld, const uint16_t* gamma,
+                              const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
+                              int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
+                              float* amax, cudaStream_t stream);
+cudaError_t launch_swiglu_amax(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
+                               int64_t ld_up, int64_t rows, int64_t cols, float* amax,
+                               cudaStream_t stream);
+// *gsf = fl(2688 / *amax), 1 for amax = 0, +inf clamped to the largest float.
+cudaError_t launch_global_scale(const float* amax, float* gsf, cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream);
 

@@ -183,14 +183,18 @@ __device__ __forceinline__ void fill_silu_table(float* table) {
   }
 }
 
+// AMAX: the abs-max pass -- y is formed the same way, its max |y| folded into
+// *amax, and nothing is quantized or stored.
+template <bool AMAX>
 __global__ void __launch_bounds__(kThreads)
 swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
               int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
-              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ amax) {
   __shared__ float inv_table[128];
   __shared__ __align__(16) float silu_table[2 * kTabHalf];
-  const float gsf = *gsf_ptr;
-  fill_inverse_scales(inv_table, gsf);
+  const float gsf = AMAX ? 0.0f : *gsf_ptr;
+  if (!AMAX) fill_inverse_scales(inv_table, gsf);
+  float run_max = 0.0f;
   fill_silu_table(silu_table);
   __syncthreads();
   const char* table = reinterpret_cast<const char*>(silu_table);
@@ -199,7 +203,7 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
   const int64_t groups = cols >> 4;
   const int64_t quads = cols >> 6;
   const int64_t segs = (groups + 31) >> 5;
-  const int64_t prows = (rows + 127) >> 7 << 7;
+  const int64_t prows = AMAX ? rows : (rows + 127) >> 7 << 7;  // the abs-max pass has no padding to write
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
 
@@ -240,6 +244,10 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       } else {
         swiglu_block<false>(gb[u], ub[u], y);
       }
+      if (AMAX) {
+        if (in_row && in_cols) run_max = fmaxf(run_max, block_amax(y));
+        continue;
+      }
       Quantized q = quantize_block(y, gsf, inv_table);
       if (!in_row) q.sf = 0;
       if (in_row && in_cols)
@@ -256,6 +264,7 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       }
     }
   }
+  if (AMAX) commit_amax(run_max, amax, inv_table);  // inv_table is unused in this mode
 }
 
 }  // namespace
@@ -266,11 +275,29 @@ cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t*
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel), kThreads, 0,
-                                      (work + kWarps - 1) / kWarps, &blocks);
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false>), kThreads,
+                                      0, (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
-  swiglu_kernel<<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf, codes,
-                                                 scales);
+  swiglu_kernel<false><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf,
+                                                        codes, scales, nullptr);
+  return cudaGetLastError();
+}
+
+}  // namespace h3q
+
+namespace h3q {
+
+cudaError_t launch_swiglu_amax(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
+                               int64_t ld_up, int64_t rows, int64_t cols, float* amax,
+                               cudaStream_t stream) {
+  const int64_t segs = (cols / 16 + 31) / 32;
+  const int64_t work = rows * segs;  // no padding rows to visit
+  int blocks = 0;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<true>), kThreads,
+                                      0, (work + kWarps - 1) / kWarps, &blocks);
+  if (err != cudaSuccess) return err;
+  swiglu_kernel<true><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, nullptr,
+                                                       nullptr, nullptr, amax);
   return cudaGetLastError();
 }
 

@@ -113,3 +113,39 @@ def test_python_binding_refuses_host_tensors():
     x = torch.zeros((4, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         h3q.h3q_quantize_nvfp4(x, torch.ones(1))
+
+
+def test_dynamic_scale_calls_reject_bad_arguments_on_the_host(lib):
+    # h3q_amax_bf16(x, ld, rows, cols, amax, stream)
+    assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, None, None) == 1
+    assert "amax" in h3q.h3q_last_error()
+    assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, 0x200002, None) == 1
+    assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, 0x100010, None) == 1  # inside x
+    assert lib.h3q_amax_bf16(0x100000, 256, 4, 100, 0x200000, None) == 1
+    assert lib.h3q_amax_bf16(None, 256, 0, 256, None, None) == h3q.H3Q_OK  # no rows: no-op
+    # h3q_rmsnorm_adaln_amax(x, ld, gamma, table, frames, row_frame, rpf, eps, rows, cols, amax, stream)
+    args = [0x100000, 256, 0x200000, 0x300000, 4, None, 16, 1e-6, 64, 256, 0x400000, None]
+    bad = list(args); bad[6] = 15
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "modulation table" in h3q.h3q_last_error()
+    bad = list(args); bad[10] = None
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1
+    bad = list(args); bad[10] = 0x300004  # inside the table
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "overlaps" in h3q.h3q_last_error()
+    bad = list(args); bad[7] = -1.0
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1
+    # h3q_swiglu_amax(gate, ldg, up, ldu, rows, cols, amax, stream)
+    assert lib.h3q_swiglu_amax(0x100000, 256, None, 256, 8, 256, 0x400000, None) == 1
+    assert lib.h3q_swiglu_amax(0x100000, 256, 0x200000, 256, 8, 256, 0x200100, None) == 1
+    # h3q_global_scale_from_amax(amax, gsf, stream)
+    assert lib.h3q_global_scale_from_amax(None, 0x100000, None) == 1
+    assert lib.h3q_global_scale_from_amax(0x100000, None, None) == 1
+    assert lib.h3q_global_scale_from_amax(0x100001, 0x100000, None) == 1
+
+
+def test_dynamic_scale_call_without_a_gpu_reports_a_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, 0x200000, None) == h3q.H3Q_ERR_CUDA
+    assert lib.h3q_global_scale_from_amax(0x100000, 0x200000, None) == h3q.H3Q_ERR_CUDA

@@ -3,14 +3,21 @@ kernel's sources hash to the value recorded beside it, and the byte counts."""
 import bench
 
 
-def test_recorded_traffic_follows_the_source_hash(monkeypatch):
-    value = bench.recorded_traffic("adaln_block_kernel")
-    assert value is not None and value > 0
-    # ~ the algorithmic bytes of the 65,280 x 7,168 workload (reads once, writes partly in L2)
-    assert 0.8 * bench.adaln_bytes(65280, 7168, 32) < value < 1.2 * bench.adaln_bytes(65280, 7168, 32)
+def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash("adaln_block_kernel")
+    record = tmp_path / "dram_traffic.txt"
+    record.write_text(f"# comment line\nadaln_block_kernel {h} 1106380800\n")
+    assert bench.recorded_traffic("adaln_block_kernel", str(record)) == 1106380800
+    assert bench.recorded_traffic("swiglu_kernel", str(record)) is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0" * 16)
-    assert bench.recorded_traffic("adaln_block_kernel") is None
-    assert bench.recorded_traffic("no_such_kernel") is None
+    assert bench.recorded_traffic("adaln_block_kernel", str(record)) is None
+    assert bench.recorded_traffic("adaln_block_kernel", str(tmp_path / "missing.txt")) is None
+
+
+def test_source_hash_covers_the_kernel_and_the_shared_header():
+    assert bench.KERNEL_SOURCES["adaln_block_kernel"] == ("adaln.cu", "h3q_device.cuh")
+    assert len(bench.kernel_source_hash("swiglu_kernel")) == 16
+    assert bench.kernel_source_hash("swiglu_kernel") != bench.kernel_source_hash("quantize_kernel")
 
 
 def test_algorithmic_bytes():
