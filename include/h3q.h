@@ -213,6 +213,28 @@ int h3q_swiglu_amax(const void *gate, int64_t ld_gate, const void *up, int64_t l
 
 int h3q_global_scale_from_amax(const float *amax, float *global_scale, void *stream);
 
+/*
+ * Dynamic quantize that needs no scratch from the caller and allocates nothing.
+ * No page has a counterpart: it is this library's convenience form of the
+ * dynamic scale above for the standalone quantize.  On the stream it runs an
+ * abs-max pass over x whose CTAs write their partial maxima into a fixed
+ * device array inside the library (a file-scope __device__ array of 4,096
+ * floats, one per device, its address resolved once per device), reduces them
+ * into *global_scale = fl(2688 / max |x|) (0 -> 1, +inf clamped), and then
+ * quantizes x as h3q_quantize_nvfp4 does with that scale.  Outputs: codes,
+ * scales and the global scale used (a device fp32 scalar written here).
+ *
+ * Limit: a shape whose abs-max pass needs more than 4,096 partial maxima (CTAs)
+ * is rejected with H3Q_ERR_INVALID_ARGUMENT; on one GPU the pass launches at
+ * most its occupancy times the SM count (1,216 CTAs on a 152-SM GB300).
+ * Calls that overlap on one device (different streams, or threads without
+ * ordering between them) share the array and race; order them on one stream.
+ * Other preconditions and status codes as h3q_quantize_nvfp4.
+ */
+int h3q_quantize_nvfp4_dynamic(const void *x, int64_t ld_x, int64_t rows, int64_t cols,
+                               float *global_scale, uint8_t *codes, uint8_t *scales,
+                               void *stream);
+
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char *h3q_last_error(void);
 

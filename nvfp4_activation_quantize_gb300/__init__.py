@@ -23,6 +23,7 @@ __all__ = [
     "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
+    "h3q_quantize_nvfp4_dynamic",
 ]
 
 H3Q_OK = 0
@@ -41,6 +42,7 @@ _SIGNATURES = {
     "h3q_rmsnorm_adaln_amax": [_P, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _I64, _I64, _P, _P],
     "h3q_swiglu_amax": [_P, _I64, _P, _I64, _I64, _I64, _P, _P],
     "h3q_global_scale_from_amax": [_P, _P, _P],
+    "h3q_quantize_nvfp4_dynamic": [_P, _I64, _I64, _I64, _P, _P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -347,3 +349,24 @@ def h3q_global_scale_from_amax(amax, global_scale=None, stream=None):
                                                   _stream(stream, dev))
     _check("h3q_global_scale_from_amax", rc)
     return global_scale
+
+
+def h3q_quantize_nvfp4_dynamic(x, global_scale=None, codes=None, scales=None, stream=None):
+    """NVFP4 of bf16 x [rows, cols] under its own per-call abs-max scale, with the
+    abs-max pass's scratch inside the library (no caller scratch, no allocation
+    there).  Returns (codes, scales, global_scale); global_scale is the fp32 device
+    scalar the call wrote.  Calls overlapping on one device race on that scratch."""
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    dev = x.device
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    if global_scale is None:
+        global_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_quantize_nvfp4_dynamic(x.data_ptr(), ld, rows, cols,
+                                                  global_scale.data_ptr(), codes.data_ptr(),
+                                                  scales.data_ptr(), _stream(stream, dev))
+    _check("h3q_quantize_nvfp4_dynamic", rc)
+    return codes, scales, global_scale

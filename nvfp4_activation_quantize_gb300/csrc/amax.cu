@@ -11,6 +11,7 @@
 // global_scale_kernel turns an abs-max into the global scale fl(2688 / amax),
 // with 0 -> 1 and +inf clamped to the largest finite binary32 first.
 #include <cfloat>
+#include <mutex>
 
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
@@ -60,7 +61,106 @@ __global__ void global_scale_kernel(const float* __restrict__ amax, float* __res
   *gsf = a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
 }
 
+// --- dynamic quantize without caller scratch -----------------------------------
+
+// Per-CTA partial maxima of h3q_quantize_nvfp4_dynamic: a file-scope device
+// array, so the call needs no scratch from the caller and allocates nothing.
+// One array per device (per context); calls that overlap on the device share it.
+__device__ __align__(256) float g_partial_amax[kMaxDynamicPartials];
+
+// Each CTA writes its own max |x| to partial[blockIdx.x] (no atomics, nothing to
+// zero beforehand).
+__global__ void __launch_bounds__(kThreads)
+amax_partials_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
+                     float* __restrict__ partial) {
+  __shared__ float scratch[32];
+  const int lane = threadIdx.x & 31;
+  const int64_t groups = cols >> 4;
+  const int64_t segs = (groups + 31) >> 5;
+  const int64_t total = rows * segs;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  float m = 0.0f;
+  for (int64_t s0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); s0 < total;
+       s0 += nwarps * kUnroll) {
+    Block16 in[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t s = s0 + u * nwarps;
+      const int64_t row = s / segs;
+      const int64_t g = (s - row * segs) * 32 + lane;
+      if (s < total && g < groups) {
+        load_stream(x + row * ld + g * kBlock, in[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) in[u].w[i] = 0;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) m = fmaxf(m, block_amax(in[u]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) scratch[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.0f;
+    for (int w = 0; w < kWarps; ++w) v = fmaxf(v, scratch[w]);
+    partial[blockIdx.x] = v;
+  }
+}
+
+// One CTA: the maximum of n partial maxima, then the global scale from it.
+__global__ void __launch_bounds__(256)
+scale_from_partials_kernel(const float* __restrict__ partial, int n, float* __restrict__ gsf) {
+  __shared__ float scratch[8];
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partial[i]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.0f;
+    for (int w = 0; w < 8; ++w) a = fmaxf(a, scratch[w]);
+    if (a > FLT_MAX) a = FLT_MAX;
+    *gsf = a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
+  }
+}
+
 }  // namespace
+
+cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks) {
+  const int64_t segs = (cols / 16 + 31) / 32;
+  return persistent_blocks(reinterpret_cast<const void*>(&amax_partials_kernel), kThreads, 0,
+                           (rows * segs + kWarps - 1) / kWarps, blocks);
+}
+
+cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
+                                        int blocks, float* gsf, cudaStream_t stream) {
+  // The device address of this context's scratch array, resolved once per device.
+  static std::mutex mutex;
+  static float* address[64] = {};
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  float* partial = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mutex);
+    if (address[device] == nullptr) {
+      void* p = nullptr;
+      err = cudaGetSymbolAddress(&p, g_partial_amax);
+      if (err != cudaSuccess) return err;
+      address[device] = static_cast<float*>(p);
+    }
+    partial = address[device];
+  }
+  amax_partials_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, partial);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  scale_from_partials_kernel<<<1, 256, 0, stream>>>(partial, blocks, gsf);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_amax_bf16(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
                              float* amax, cudaStream_t stream) {

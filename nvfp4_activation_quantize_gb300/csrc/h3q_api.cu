@@ -314,6 +314,37 @@ int h3q_global_scale_from_amax(const float* amax, float* global_scale, void* str
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_quantize_nvfp4_dynamic(const void* x, int64_t ld_x, int64_t rows, int64_t cols,
+                               float* global_scale, uint8_t* codes, uint8_t* scales,
+                               void* stream) {
+  static const char* fn = "h3q_quantize_nvfp4_dynamic";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  const Span in = span(x, view_bytes(rows, cols, ld_x));
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span s = span(scales, h3q_scale_bytes(rows, cols));
+  const Span g = span(global_scale, 4);
+  if (overlap(in, c) || overlap(in, s) || overlap(c, s) || overlap(g, in) || overlap(g, c) ||
+      overlap(g, s))
+    return invalid(fn, "outputs overlap an input or each other");
+  int blocks = 0;
+  cudaError_t err = h3q::dynamic_scale_partials(rows, cols, &blocks);
+  if (err != cudaSuccess) return cuda_failed(fn, err);
+  if (blocks > h3q::kMaxDynamicPartials)
+    return fail(H3Q_ERR_INVALID_ARGUMENT, "%s: the abs-max pass needs %d partial maxima, more than "
+                "the %d the static scratch holds", fn, blocks, h3q::kMaxDynamicPartials);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  err = h3q::launch_dynamic_scale_static(static_cast<const uint16_t*>(x), ld_x, rows, cols, blocks,
+                                         global_scale, st);
+  if (err != cudaSuccess) return cuda_failed(fn, err);
+  err = h3q::launch_quantize(static_cast<const uint16_t*>(x), ld_x, rows, cols, global_scale, codes,
+                             scales, st);
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
                          const float* global_scale, float* out, void* stream) {
   static const char* fn = "h3q_dequantize_nvfp4";

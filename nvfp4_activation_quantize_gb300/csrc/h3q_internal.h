@@ -41,6 +41,15 @@ cudaError_t launch_swiglu_amax(const uint16_t* gate, int64_t ld_gate, const uint
 // *gsf = fl(2688 / *amax), 1 for amax = 0, +inf clamped to the largest float.
 cudaError_t launch_global_scale(const float* amax, float* gsf, cudaStream_t stream);
 
+// Dynamic quantize without caller scratch: per-CTA partial maxima in a
+// file-scope device array of kMaxDynamicPartials floats.  dynamic_scale_partials
+// gives the number of CTAs (partials) the abs-max pass launches for a shape;
+// launch_dynamic_scale_static runs that pass and writes the global scale.
+constexpr int kMaxDynamicPartials = 4096;
+cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks);
+cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
+                                        int blocks, float* gsf, cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream);
 
