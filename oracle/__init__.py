@@ -68,6 +68,8 @@ _SIGNATURES = {
     "orc_quantize_block": ([_P, _F, _P, _P], None),
     "orc_global_scale": ([_F], _F),
     "orc_amax_bf16": ([_P, _I64], _F),
+    "orc_row_rstd_f32": ([_P, _I64, _F], _F),
+    "orc_residual_adaln_rows": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P], None),
     "orc_global_scale_from_amax": ([_F], _F),
     "orc_scale_offset": ([_I64, _I64, _I64], _I64),
     "orc_padded_rows": ([_I64], _I64),
@@ -305,6 +307,55 @@ def adaln_rows(x_bits, gamma_bits, table_bits, frames, eps: float, gsf: float | 
 
     _run(work, n, threads)
     return codes, sf, rstd, y
+
+
+def row_rstd_f32(row: np.ndarray, eps: float) -> float:
+    """rstd of one fp32 row in the canonical order (squares of fp32 values)."""
+    r = np.ascontiguousarray(row, dtype=np.float32).ravel()
+    _check_cols(r.size)
+    return float(lib().orc_row_rstd_f32(_ptr(r), r.size, float(eps)))
+
+
+def residual_adaln_rows(h, o_bits, bias_bits, gate_bits, gamma_bits, table_bits, frames, eps: float,
+                        gsf: float | None, want_y: bool = False, threads: int = 1):
+    """Residual fold + RMSNorm + AdaLN -> NVFP4 (NEXT row f1).
+
+    ``h`` fp32 [n, cols] (not modified; the folded residual is returned), ``o``
+    bf16 bits [n, cols], ``bias`` bf16 bits [cols] or None, ``gate`` bf16 bits
+    [T, cols], ``table`` [T, 2, cols]; ``frames[i]`` indexes both tables.
+    Returns (h_out, codes, sf, rstd, y)."""
+    h_out = np.array(h, dtype=np.float32, copy=True, order="C")
+    o = _u16(o_bits)
+    n, cols = o.shape
+    _check_cols(cols)
+    assert h_out.shape == (n, cols)
+    bias = None if bias_bits is None else _u16(bias_bits).reshape(cols)
+    gate = _u16(gate_bits)
+    assert gate.ndim == 2 and gate.shape[1] == cols
+    gamma = _u16(gamma_bits).reshape(cols)
+    table = _u16(table_bits)
+    assert table.ndim == 3 and table.shape[1:] == (2, cols) and table.shape[0] == gate.shape[0]
+    frames = np.ascontiguousarray(frames, dtype=np.int64).reshape(n)
+    if n and (frames.min() < 0 or frames.max() >= table.shape[0]):
+        raise ValueError("frame index outside [0, frames)")
+    quant = gsf is not None
+    codes = np.empty((n, cols // 2), np.uint8) if quant else None
+    sf = np.empty((n, cols // 16), np.uint8) if quant else None
+    rstd = np.empty(n, np.float32)
+    y = np.empty((n, cols), np.uint16) if want_y else None
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(cols, np.float32)
+        lib().orc_residual_adaln_rows(
+            _ptr(h_out[a:b]), b - a, cols, cols, _ptr(o[a:b]), cols,
+            _ptr(bias) if bias is not None else None, _ptr(gate), _ptr(gamma), _ptr(table),
+            _ptr(frames[a:b]), float(eps), float(gsf if quant else 1.0), _ptr(scratch),
+            _ptr(codes[a:b]) if quant else None, _ptr(sf[a:b]) if quant else None,
+            _ptr(rstd[a:b]), _ptr(y[a:b]) if want_y else None)
+
+    _run(work, n, threads)
+    return h_out, codes, sf, rstd, y
 
 
 def swiglu_rows(gate_bits, up_bits, gsf: float | None, want_y: bool = False, threads: int = 1):

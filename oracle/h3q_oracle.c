@@ -456,6 +456,90 @@ void orc_adaln_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t ld,
 
 /* (b) SwiGLU silu(gate) * up, then NVFP4 ([TRT] SiLU-and-mul producer;
  * [FV-CUH] swiglu_bf16).  y_out as above. */
+/* ------------------------------------------------------------------------ */
+/* Residual fold + RMSNorm + AdaLN (NEXT row f1)                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * [TRT] commit "...norm1 ... from a second table": a block folds its MLP
+ * residual into the next block's norm1 kernel, reading the gate from its own
+ * AdaLN table while the scale and shift come from the next block's.
+ * [FV-API] residual_norm_quantize: in place h += bf16(o + bias) * scale on a
+ * contiguous fp32 residual h, then NVFP4 of the normed h.
+ *
+ * Reading: with the gate g[t] of the row's frame (bf16 table [T, cols]),
+ *   u = bf16(fl(o + bias))   (u = o when there is no bias)
+ *   h' = fl(h + fl(u * g))   written back to h
+ * and then the RMSNorm + AdaLN spec above on the fp32 values h' (the same
+ * canonical reduction order, squares by fmaf of fp32 values).
+ */
+float orc_row_rstd_f32(const float *row, int64_t cols, float eps)
+{
+    int64_t chunks = cols / 8;
+    float lane[128];
+    for (int l = 0; l < 128; ++l) {
+        float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int64_t c = l; c < chunks; c += 128)
+            for (int e = 0; e < 8; ++e) {
+                float v = row[8 * c + e];
+                p[e] = fmaf(v, v, p[e]);
+            }
+        lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+    }
+    float group[4];
+    for (int w = 0; w < 4; ++w) {
+        float g[32];
+        memcpy(g, lane + 32 * w, sizeof g);
+        for (int o = 16; o >= 1; o /= 2) {
+            float next[32];
+            for (int l = 0; l < 32; ++l)
+                next[l] = g[l] + g[l ^ o];
+            memcpy(g, next, sizeof g);
+        }
+        group[w] = g[0];
+    }
+    float ss = (group[0] + group[1]) + (group[2] + group[3]);
+    float mean = ss / (float)cols;
+    float root = sqrtf(mean + eps);
+    return 1.0f / root;
+}
+
+void orc_residual_adaln_rows(float *h, int64_t nrows, int64_t cols, int64_t ld_h,
+                             const uint16_t *o, int64_t ld_o, const uint16_t *bias,
+                             const uint16_t *gate, const uint16_t *gamma, const uint16_t *table,
+                             const int64_t *frame_of_row, float eps, float gsf, float *scratch_row,
+                             uint8_t *codes, uint8_t *sf, float *rstd_out, uint16_t *y_out)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        float *hr = h + r * ld_h;
+        const uint16_t *orow = o + r * ld_o;
+        const uint16_t *g = gate + frame_of_row[r] * cols;
+        for (int64_t j = 0; j < cols; ++j) {
+            float u = bias ? orc_bf16_round(orc_bf16_value(orow[j]) + orc_bf16_value(bias[j]))
+                           : orc_bf16_value(orow[j]);
+            float t = u * orc_bf16_value(g[j]);
+            hr[j] = hr[j] + t;
+        }
+        float rstd = orc_row_rstd_f32(hr, cols, eps);
+        const uint16_t *shift = table + frame_of_row[r] * 2 * cols;
+        const uint16_t *scale = shift + cols;
+        for (int64_t j = 0; j < cols; ++j) {
+            float n = hr[j] * rstd;
+            float hh = n * orc_bf16_value(gamma[j]);
+            float a = 1.0f + orc_bf16_value(scale[j]);
+            float m = hh * a;
+            float out = m + orc_bf16_value(shift[j]);
+            scratch_row[j] = orc_bf16_round(out);
+            if (y_out)
+                y_out[r * cols + j] = orc_bf16_bits(out);
+        }
+        if (rstd_out)
+            rstd_out[r] = rstd;
+        if (codes)
+            quantize_row_values(scratch_row, cols, gsf, codes + r * (cols / 2),
+                                sf + r * (cols / 16));
+    }
+}
+
 void orc_swiglu_rows(const uint16_t *gate, int64_t ld_gate, const uint16_t *up, int64_t ld_up,
                      int64_t nrows, int64_t cols, float gsf, float *scratch_row, uint8_t *codes,
                      uint8_t *sf, uint16_t *y_out)
