@@ -75,6 +75,11 @@ def swiglu_bytes(rows: int, cols: int) -> int:
     return 4 * rows * cols + out_bytes(rows, cols) + 4
 
 
+def residual_bytes(rows: int, cols: int, frames: int) -> int:
+    # h read and written (fp32), o read, codes + scales, bias + gamma, gate and modulation tables
+    return (4 + 4 + 2) * rows * cols + out_bytes(rows, cols) + 2 * 2 * cols + frames * 3 * cols * 2 + 4
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -446,6 +451,23 @@ def measure_producers(h3q, dev, stream, args):
                                                      "twice, GB/s by the single-pass bytes")
     del w, c, s
 
+    # residual fold + RMSNorm + AdaLN: h (fp32) is read and written back each launch
+    w = workloads.residual_inputs(dev)
+    g = torch.tensor([90.0], dtype=torch.float32, device=dev)
+    c = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
+
+    def residual_step():
+        h3q.h3q_residual_rmsnorm_adaln_nvfp4(w["h"], w["o"], w["gate"], w["gamma"], w["table"], g,
+                                             bias=w["bias"], rows_per_frame=RPF, eps=w["eps"],
+                                             codes=c, scales=s, stream=stream)
+
+    for _ in range(3):
+        residual_step()
+    _, per = time_launches(residual_step, n, stream)
+    res["residual_adaln_65280x7168"] = entry(residual_bytes(ROWS, COLS, FRAMES), per, ROWS)
+    del w, c, s
+
     # standalone quantize 8,192 x 7,168 (150 MB: near L2, so L2 is flushed before each launch)
     x = workloads.quantize_inputs(dev)
     g = torch.tensor([2688.0 / float(x.float().abs().max())], dtype=torch.float32, device=dev)
@@ -559,6 +581,16 @@ def run_single(args, dev):
         c, s = h3q.h3q_swiglu_nvfp4(gate, up, g, stream=stream)
         fn = lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)  # noqa: E731
         nbytes = swiglu_bytes(rows, workloads.FFN)
+    elif kind == "residual":
+        rows = args.rows or ROWS
+        w = workloads.residual_inputs(dev, rows=rows, frames=max(1, -(-rows // RPF)))
+        g = torch.tensor([90.0], dtype=torch.float32, device=dev)
+        c = torch.empty((rows, COLS // 2), dtype=torch.uint8, device=dev)
+        s = torch.empty((padded(rows), COLS // 16), dtype=torch.uint8, device=dev)
+        fn = lambda: h3q.h3q_residual_rmsnorm_adaln_nvfp4(  # noqa: E731
+            w["h"], w["o"], w["gate"], w["gamma"], w["table"], g, bias=w["bias"], rows_per_frame=RPF,
+            eps=w["eps"], codes=c, scales=s, stream=stream)
+        nbytes = residual_bytes(rows, COLS, w["table"].shape[0])
     else:
         rows = args.rows or ROWS
         x = workloads.attention_output(dev, tokens=rows)
@@ -591,7 +623,7 @@ def main(argv=None):
     p.add_argument("--reference-rows", type=int, default=510)
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize"],
+    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize", "residual"],
                    help="time one producer alone (for profiling); prints a short JSON line")
     p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)

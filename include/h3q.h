@@ -174,6 +174,38 @@ int h3q_dequantize_nvfp4(const uint8_t *codes, const uint8_t *scales, int64_t ro
                          const float *global_scale, float *out, void *stream);
 
 /*
+ * Residual fold + RMSNorm + AdaLN -> NVFP4 (the residual add folded into the
+ * next norm).  TensorRT-LLM PR #21483, commit "...norm1 ... from a second
+ * table": a block folds its MLP residual into the next block's norm1 kernel,
+ * reading the gate from its own AdaLN table while the scale and shift come from
+ * the next block's.  FastVideo API page, residual_norm_quantize: in place
+ * h += bf16(o + bias) * scale on a contiguous fp32 residual, then NVFP4 of the
+ * normed h.  Per row r with frame t:
+ *   u   = bf16(fl(o + bias))           (u = o when bias is NULL)
+ *   h'  = fl(h + fl(u * gate[t]))      written back to h
+ *   then h3q_rmsnorm_adaln_nvfp4's arithmetic on the fp32 values h' (same
+ *   canonical reduction order, squares of fp32 values) and the NVFP4 quantize.
+ *
+ *   h           fp32 [rows, cols], row stride ld_h (>= cols, a multiple of 8),
+ *               32-byte aligned; read and overwritten with h'.
+ *   o           bf16 [rows, cols], row stride ld_o, as x of the other producers.
+ *   bias        bf16 [cols] or NULL.
+ *   gate_table  bf16 [num_frames, cols]: the gate of each frame (this block's).
+ *   gamma, mod_table, num_frames, row_frame, rows_per_frame, eps, global_scale,
+ *   codes, scales, row_rstd: as h3q_rmsnorm_adaln_nvfp4 (the next block's
+ *               modulation table; the frame of a row indexes both tables).
+ * Limits: cols <= 8,192.  h, codes, scales and row_rstd must not overlap an
+ * input or each other.  Status codes as the other producers.
+ */
+int h3q_residual_rmsnorm_adaln_nvfp4(float *h, int64_t ld_h, const void *o, int64_t ld_o,
+                                     const void *bias, const void *gate_table, const void *gamma,
+                                     const void *mod_table, int64_t num_frames,
+                                     const int32_t *row_frame, int64_t rows_per_frame, float eps,
+                                     int64_t rows, int64_t cols, const float *global_scale,
+                                     uint8_t *codes, uint8_t *scales, float *row_rstd,
+                                     void *stream);
+
+/*
  * Dynamic and calibrated global scales.
  *
  * FastVideo API page, NVFP4DecoderLinear: a dynamic layer scales each call by

@@ -23,7 +23,7 @@ __all__ = [
     "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
-    "h3q_quantize_nvfp4_dynamic",
+    "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4",
 ]
 
 H3Q_OK = 0
@@ -43,6 +43,8 @@ _SIGNATURES = {
     "h3q_swiglu_amax": [_P, _I64, _P, _I64, _I64, _I64, _P, _P],
     "h3q_global_scale_from_amax": [_P, _P, _P],
     "h3q_quantize_nvfp4_dynamic": [_P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "h3q_residual_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _I64,
+                                         ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -370,3 +372,55 @@ def h3q_quantize_nvfp4_dynamic(x, global_scale=None, codes=None, scales=None, st
                                                   scales.data_ptr(), _stream(stream, dev))
     _check("h3q_quantize_nvfp4_dynamic", rc)
     return codes, scales, global_scale
+
+
+def h3q_residual_rmsnorm_adaln_nvfp4(h, o, gate_table, gamma, mod_table, global_scale, *, bias=None,
+                                     row_frame=None, rows_per_frame=None, eps=1e-6, codes=None,
+                                     scales=None, row_rstd=None, stream=None):
+    """Residual fold + RMSNorm + AdaLN -> NVFP4: h (fp32 [rows, cols], updated in place)
+    += bf16(o + bias) * gate_table[frame], then the AdaLN producer on the folded h.
+    ``gate_table`` bf16 [frames, cols]; ``mod_table`` bf16 [frames, 2, cols].
+    Returns (codes, scales)."""
+    import torch
+
+    _cuda_tensor("h", h, torch.float32)
+    dev = h.device
+    if h.dim() != 2 or (h.shape[1] > 1 and h.stride(1) != 1):
+        raise ValueError("h must be 2-D with contiguous rows")
+    rows, cols = h.shape
+    ld_h = h.stride(0) if rows > 1 else cols
+    o, rows_o, cols_o, ld_o = _rows_view("o", o, torch.bfloat16, dev)
+    if (rows_o, cols_o) != (rows, cols):
+        raise ValueError("o must have the shape of h")
+    bias_ptr = None
+    if bias is not None:
+        _contiguous("bias", bias, torch.bfloat16, (cols,), dev)
+        bias_ptr = bias.data_ptr()
+    _cuda_tensor("gate_table", gate_table, torch.bfloat16, dev)
+    if gate_table.dim() != 2 or gate_table.shape[1] != cols or not gate_table.is_contiguous():
+        raise ValueError("gate_table must be contiguous [frames, cols]")
+    _contiguous("gamma", gamma, torch.bfloat16, (cols,), dev)
+    _cuda_tensor("mod_table", mod_table, torch.bfloat16, dev)
+    if (mod_table.dim() != 3 or mod_table.shape[1:] != (2, cols) or not mod_table.is_contiguous()
+            or mod_table.shape[0] != gate_table.shape[0]):
+        raise ValueError("mod_table must be contiguous [frames, 2, cols], frames as gate_table")
+    rf_ptr = None
+    if row_frame is not None:
+        _contiguous("row_frame", row_frame, torch.int32, (rows,), dev)
+        rf_ptr = row_frame.data_ptr()
+        rows_per_frame = 0
+    elif rows_per_frame is None:
+        raise ValueError("give row_frame or rows_per_frame")
+    rstd_ptr = None
+    if row_rstd is not None:
+        _contiguous("row_rstd", row_rstd, torch.float32, (rows,), dev)
+        rstd_ptr = row_rstd.data_ptr()
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_residual_rmsnorm_adaln_nvfp4(
+            h.data_ptr(), ld_h, o.data_ptr(), ld_o, bias_ptr, gate_table.data_ptr(), gamma.data_ptr(),
+            mod_table.data_ptr(), mod_table.shape[0], rf_ptr, int(rows_per_frame), float(eps), rows,
+            cols, gsf.data_ptr(), codes.data_ptr(), scales.data_ptr(), rstd_ptr, _stream(stream, dev))
+    _check("h3q_residual_rmsnorm_adaln_nvfp4", rc)
+    return codes, scales

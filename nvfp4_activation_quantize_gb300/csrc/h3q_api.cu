@@ -229,6 +229,62 @@ int h3q_swiglu_nvfp4(const void* gate, int64_t ld_gate, const void* up, int64_t 
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_residual_rmsnorm_adaln_nvfp4(float* h, int64_t ld_h, const void* o, int64_t ld_o,
+                                     const void* bias, const void* gate_table, const void* gamma,
+                                     const void* mod_table, int64_t num_frames,
+                                     const int32_t* row_frame, int64_t rows_per_frame, float eps,
+                                     int64_t rows, int64_t cols, const float* global_scale,
+                                     uint8_t* codes, uint8_t* scales, float* row_rstd,
+                                     void* stream) {
+  static const char* fn = "h3q_residual_rmsnorm_adaln_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (cols > 8192) return invalid(fn, "cols exceeds 8,192");
+  if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
+  if (num_frames < 1) return invalid(fn, "num_frames must be >= 1");
+  if (num_frames > (int64_t(1) << 31)) return invalid(fn, "num_frames exceeds 2^31");
+  if (rows == 0) return H3Q_OK;
+  if (h == nullptr || !aligned(h, 32)) return invalid(fn, "h must be a 32-byte aligned pointer");
+  if (ld_h < cols || ld_h % 8 != 0) return invalid(fn, "ld of h must be >= cols and a multiple of 8");
+  if (ld_h > (int64_t(1) << 61) / rows) return invalid(fn, "h: rows * ld overflows");
+  if (int e = check_input(fn, "o", o, ld_o, rows, cols)) return e;
+  if (bias != nullptr)
+    if (int e = check_input(fn, "bias", bias, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "gate_table", gate_table, cols, num_frames, cols)) return e;
+  if (int e = check_input(fn, "gamma", gamma, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "mod_table", mod_table, cols, 2 * num_frames, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  if (row_frame != nullptr) {
+    if (!aligned(row_frame, 4)) return invalid(fn, "row_frame must be 4-byte aligned");
+  } else {
+    if (rows_per_frame < 1) return invalid(fn, "rows_per_frame must be >= 1 when row_frame is NULL");
+    if ((rows - 1) / rows_per_frame >= num_frames)
+      return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
+  }
+  if (row_rstd != nullptr && !aligned(row_rstd, 4)) return invalid(fn, "row_rstd must be 4-byte aligned");
+  const Span hs = span(h, ((rows - 1) * ld_h + cols) * 4);
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span sc = span(scales, h3q_scale_bytes(rows, cols));
+  const Span r = row_rstd ? span(row_rstd, rows * 4) : Span{0, 0};
+  const Span ins[7] = {span(o, view_bytes(rows, cols, ld_o)), bias ? span(bias, cols * 2) : Span{0, 0},
+                       span(gate_table, num_frames * 2 * cols), span(gamma, cols * 2),
+                       span(mod_table, num_frames * 4 * cols),
+                       row_frame ? span(row_frame, rows * 4) : Span{0, 0}, span(global_scale, 4)};
+  const Span outs[4] = {hs, c, sc, r};
+  for (int i = 0; i < 4; ++i) {
+    for (const Span& in : ins)
+      if (overlap(outs[i], in)) return invalid(fn, "an output (h, codes, scales, row_rstd) overlaps an input");
+    for (int k = i + 1; k < 4; ++k)
+      if (overlap(outs[i], outs[k])) return invalid(fn, "outputs overlap each other");
+  }
+  cudaError_t err = h3q::launch_residual_adaln(
+      h, ld_h, static_cast<const uint16_t*>(o), ld_o, static_cast<const uint16_t*>(bias),
+      static_cast<const uint16_t*>(gate_table), static_cast<const uint16_t*>(gamma),
+      static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, eps, rows,
+      cols, global_scale, codes, scales, row_rstd, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 // --- dynamic and calibrated scales ------------------------------------------
 
 namespace {

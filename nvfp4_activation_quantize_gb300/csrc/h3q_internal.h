@@ -50,6 +50,14 @@ cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks);
 cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
                                         int blocks, float* gsf, cudaStream_t stream);
 
+// Residual fold + RMSNorm + AdaLN -> NVFP4 (rows of at most 8,192 columns).
+cudaError_t launch_residual_adaln(float* h, int64_t ld_h, const uint16_t* o, int64_t ld_o,
+                                  const uint16_t* bias, const uint16_t* gate, const uint16_t* gamma,
+                                  const uint16_t* table, int64_t num_frames,
+                                  const int32_t* row_frame, int64_t rows_per_frame, float eps,
+                                  int64_t rows, int64_t cols, const float* gsf, uint8_t* codes,
+                                  uint8_t* scales, float* row_rstd, cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream);
 

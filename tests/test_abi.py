@@ -149,3 +149,30 @@ def test_dynamic_scale_call_without_a_gpu_reports_a_cuda_error(lib):
         pytest.skip("a GPU is present")
     assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, 0x200000, None) == h3q.H3Q_ERR_CUDA
     assert lib.h3q_global_scale_from_amax(0x100000, 0x200000, None) == h3q.H3Q_ERR_CUDA
+
+
+def test_residual_fold_rejects_bad_arguments_on_the_host(lib):
+    # (h, ld_h, o, ld_o, bias, gate, gamma, table, frames, row_frame, rpf, eps, rows, cols,
+    #  gsf, codes, scales, row_rstd, stream)
+    good = [0x1000000, 256, 0x2000000, 256, None, 0x3000000, 0x3100000, 0x3200000, 4, None, 16,
+            1e-6, 64, 256, 0x4000000, 0x5000000, 0x6000000, None, None]
+    f = lib.h3q_residual_rmsnorm_adaln_nvfp4
+
+    def call(**kw):
+        a = list(good)
+        names = ["h", "ld_h", "o", "ld_o", "bias", "gate", "gamma", "table", "frames", "row_frame",
+                 "rpf", "eps", "rows", "cols", "gsf", "codes", "scales", "rstd", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(cols=16384, ld_h=16384, ld_o=16384) == 1 and "8,192" in h3q.h3q_last_error()
+    assert call(h=None) == 1
+    assert call(h=0x1000010) == 1                       # h not 32-byte aligned
+    assert call(ld_h=260) == 1                          # ld_h not a multiple of 8
+    assert call(gate=None) == 1
+    assert call(bias=0x3000010) == 1                    # bias not 32-byte aligned
+    assert call(rpf=15) == 1 and "modulation table" in h3q.h3q_last_error()
+    assert call(o=0x1000000 + 512) == 1 and "overlap" in h3q.h3q_last_error()   # o inside h
+    assert call(codes=0x1000000 + 4096) == 1                                     # codes inside h
+    assert call(rows=0, h=None, o=None) == h3q.H3Q_OK

@@ -76,6 +76,28 @@ def adaln_inputs(device, rows: int = TOKENS, cols: int = HIDDEN, frames: int = F
     return {"x": x, "gamma": gamma, "table": table, "rows_per_frame": rows_per_frame, "eps": 1e-6}
 
 
+def residual_inputs(device, rows: int = TOKENS, cols: int = HIDDEN, frames: int = FRAMES,
+                    rows_per_frame: int = TOKENS_PER_FRAME, seed: int = 6, bias: bool = True) -> dict:
+    """Residual fold + RMSNorm + AdaLN inputs: the fp32 residual h ~ 4 * N(0, 1) * s_j
+    with per-channel s_j ~ LogNormal(0, 0.5), the MLP output o ~ N(0, 1) (bf16), a bias
+    ~ N(0, 0.1) (bf16, or None), the gate table [frames, cols] ~ N(0, 0.3), gamma ~
+    N(1, 0.1) and the modulation table [frames, 2, cols] ~ N(0, 0.3); eps 1e-6."""
+    gen = _gen(device, seed)
+    col_scale = torch.exp(0.5 * torch.randn(cols, generator=gen, device=device, dtype=torch.float32))
+    h = torch.empty((rows, cols), dtype=torch.float32, device=device)
+    step = max(1, _CHUNK_ELEMS // max(cols, 1))
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        h[r0:r1] = torch.randn((r1 - r0, cols), generator=gen, device=device) * col_scale * 4.0
+    o = _normal_bf16(rows, cols, gen, device)
+    b = _normal_bf16(1, cols, gen, device, std=0.1).reshape(cols) if bias else None
+    gate = _normal_bf16(frames, cols, gen, device, std=0.3)
+    gamma = _normal_bf16(1, cols, gen, device, std=0.1, mean=1.0).reshape(cols)
+    table = _normal_bf16(frames * 2, cols, gen, device, std=0.3).reshape(frames, 2, cols)
+    return {"h": h, "o": o, "bias": b, "gate": gate, "gamma": gamma, "table": table,
+            "rows_per_frame": rows_per_frame, "eps": 1e-6}
+
+
 def tiny_adaln_inputs(device, seed: int = 1) -> dict:
     """The tiny bit-exactness case: x [64, 256] ~ N(0, 1), gamma ~ N(1, 0.1),
     table [4, 2, 256] ~ N(0, 0.2), row -> frame = row // 16, eps 1e-6."""
