@@ -69,6 +69,7 @@ _SIGNATURES = {
     "orc_global_scale": ([_F], _F),
     "orc_amax_bf16": ([_P, _I64], _F),
     "orc_row_rstd_f32": ([_P, _I64, _F], _F),
+    "orc_swiglu_packed_rows": ([_P, _I64, _P, _I64, _I64, _F, _P, _P, _P, _P], None),
     "orc_residual_adaln_rows": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P], None),
     "orc_global_scale_from_amax": ([_F], _F),
     "orc_scale_offset": ([_I64, _I64, _I64], _I64),
@@ -378,6 +379,31 @@ def swiglu_rows(gate_bits, up_bits, gsf: float | None, want_y: bool = False, thr
                               _ptr(codes[a:b]) if quant else None,
                               _ptr(sf[a:b]) if quant else None,
                               _ptr(y[a:b]) if want_y else None)
+
+    _run(work, n, threads)
+    return codes, sf, y
+
+
+def swiglu_packed_rows(o_bits, bias_bits, gsf: float | None, want_y: bool = False, threads: int = 1):
+    """SwiGLU of a value-first packed projection o [n, 2F] (value, then gate) plus
+    its bias [2F] (or None) -> NVFP4 of the [n, F] output. Returns (codes, sf, y)."""
+    o = _u16(o_bits)
+    n, two_f = o.shape
+    f = two_f // 2
+    _check_cols(f)
+    bias = None if bias_bits is None else _u16(bias_bits).reshape(two_f)
+    quant = gsf is not None
+    codes = np.empty((n, f // 2), np.uint8) if quant else None
+    sf = np.empty((n, f // 16), np.uint8) if quant else None
+    y = np.empty((n, f), np.uint16) if want_y else None
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(f, np.float32)
+        lib().orc_swiglu_packed_rows(_ptr(o[a:b]), two_f, _ptr(bias) if bias is not None else None,
+                                     b - a, f, float(gsf if quant else 1.0), _ptr(scratch),
+                                     _ptr(codes[a:b]) if quant else None,
+                                     _ptr(sf[a:b]) if quant else None, _ptr(y[a:b]) if want_y else None)
 
     _run(work, n, threads)
     return codes, sf, y

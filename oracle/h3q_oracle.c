@@ -456,6 +456,37 @@ void orc_adaln_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t ld,
 
 /* (b) SwiGLU silu(gate) * up, then NVFP4 ([TRT] SiLU-and-mul producer;
  * [FV-CUH] swiglu_bf16).  y_out as above. */
+/*
+ * SwiGLU of a value-first packed projection with its bias (NEXT row f2).
+ * [FV-API] swiglu_quantize: o is [M, 2F], value first (columns 0..F-1), gate
+ * second, the bias not yet added.  Reading: each half gets its bias in binary32
+ * and is rounded to bf16, as the projection's own output would be,
+ *   v = bf16(fl(o_v + b_v)),  g = bf16(fl(o_g + b_g))   (no add without a bias)
+ * and then the SwiGLU spec: y = bf16(fl(fl(g * sigma(g)) * v)), quantized.
+ */
+void orc_swiglu_packed_rows(const uint16_t *o, int64_t ld_o, const uint16_t *bias, int64_t nrows,
+                            int64_t f, float gsf, float *scratch_row, uint8_t *codes, uint8_t *sf,
+                            uint16_t *y_out)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint16_t *orow = o + r * ld_o;
+        for (int64_t j = 0; j < f; ++j) {
+            float v = orc_bf16_value(orow[j]);
+            float g = orc_bf16_value(orow[f + j]);
+            if (bias) {
+                v = orc_bf16_round(v + orc_bf16_value(bias[j]));
+                g = orc_bf16_round(g + orc_bf16_value(bias[f + j]));
+            }
+            float y = orc_swiglu_value(g, v);
+            scratch_row[j] = y;
+            if (y_out)
+                y_out[r * f + j] = orc_bf16_bits(y);
+        }
+        if (codes)
+            quantize_row_values(scratch_row, f, gsf, codes + r * (f / 2), sf + r * (f / 16));
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Residual fold + RMSNorm + AdaLN (NEXT row f1)                              */
 /* ------------------------------------------------------------------------ */
