@@ -412,7 +412,21 @@ def measure_producers(h3q, dev, stream, args):
         h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)
     _, per = time_launches(lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream), n, stream)
     res["swiglu_65280x18944"] = entry(swiglu_bytes(*gate.shape), per, gate.shape[0])
-    del gate, up, c, s
+    del c, s
+
+    # SwiGLU of the value-first packed projection with its bias, 65,280 x 2 x 18,944
+    o = torch.empty((ROWS, 2 * workloads.FFN), dtype=torch.bfloat16, device=dev)
+    o[:, :workloads.FFN], o[:, workloads.FFN:] = up, gate
+    del gate, up
+    bias = torch.zeros(2 * workloads.FFN, dtype=torch.bfloat16, device=dev).normal_(0.0, 0.2)
+    c, s = h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, stream=stream)
+    for _ in range(3):
+        h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, codes=c, scales=s, stream=stream)
+    _, per = time_launches(lambda: h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, codes=c, scales=s,
+                                                               stream=stream), n, stream)
+    res["swiglu_packed_bias_65280x18944"] = entry(swiglu_bytes(ROWS, workloads.FFN) + 4 * workloads.FFN,
+                                                  per, ROWS)
+    del o, bias, c, s
 
     # attention-output quantize: 65,280 and 300,000 tokens of 56 x 128
     for tokens in (65280, 300000):

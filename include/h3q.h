@@ -163,6 +163,21 @@ int h3q_swiglu_nvfp4(const void *gate, int64_t ld_gate, const void *up, int64_t 
                      uint8_t *scales, void *stream);
 
 /*
+ * SwiGLU of a value-first packed projection with its bias (FastVideo API page,
+ * swiglu_quantize: o [M, 2F], value first, gate second, bias not yet added).
+ * Each half gets its bias in binary32 and is rounded to bf16,
+ *   v = bf16(fl(o[:, j] + bias[j])),  g = bf16(fl(o[:, F + j] + bias[F + j])),
+ * then as h3q_swiglu_nvfp4: y = bf16(fl(fl(g * sigma(g)) * v)), quantized.
+ *
+ *   o       bf16 [rows, 2F], row stride ld_o (>= 2F, a multiple of 16), 32-byte aligned.
+ *   bias    bf16 [2F] (value biases, then gate biases), 32-byte aligned, or NULL.
+ *   f       F, a multiple of 64; codes [rows, F/2] and scales [pad128(rows), F/16].
+ */
+int h3q_swiglu_packed_nvfp4(const void *o, int64_t ld_o, const void *bias, int64_t rows,
+                            int64_t f, const float *global_scale, uint8_t *codes, uint8_t *scales,
+                            void *stream);
+
+/*
  * Dequantize (checking path): out[r][j] = fl((E2M1value(c) * E4M3value(sf)) / gsf),
  * the value a block-scaled NVFP4 GEMM with alpha = 1/gsf sees for the element.
  * No page defines it; it is the inverse the producers' consumers apply.

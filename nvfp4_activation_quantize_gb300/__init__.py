@@ -23,7 +23,7 @@ __all__ = [
     "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
-    "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4",
+    "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
 ]
 
 H3Q_OK = 0
@@ -43,6 +43,7 @@ _SIGNATURES = {
     "h3q_swiglu_amax": [_P, _I64, _P, _I64, _I64, _I64, _P, _P],
     "h3q_global_scale_from_amax": [_P, _P, _P],
     "h3q_quantize_nvfp4_dynamic": [_P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "h3q_swiglu_packed_nvfp4": [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P],
     "h3q_residual_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _I64,
                                          ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P],
 }
@@ -423,4 +424,28 @@ def h3q_residual_rmsnorm_adaln_nvfp4(h, o, gate_table, gamma, mod_table, global_
             mod_table.data_ptr(), mod_table.shape[0], rf_ptr, int(rows_per_frame), float(eps), rows,
             cols, gsf.data_ptr(), codes.data_ptr(), scales.data_ptr(), rstd_ptr, _stream(stream, dev))
     _check("h3q_residual_rmsnorm_adaln_nvfp4", rc)
+    return codes, scales
+
+
+def h3q_swiglu_packed_nvfp4(o, global_scale, bias=None, codes=None, scales=None, stream=None):
+    """SwiGLU of the value-first packed projection o [rows, 2F] (value, then gate)
+    with its bias [2F] (or None) added and rounded to bf16 first; returns (codes, scales)
+    of the [rows, F] output."""
+    import torch
+
+    o, rows, two_f, ld = _rows_view("o", o, torch.bfloat16)
+    dev = o.device
+    if two_f % 2:
+        raise ValueError("o must have an even number of columns")
+    f = two_f // 2
+    bias_ptr = None
+    if bias is not None:
+        _contiguous("bias", bias, torch.bfloat16, (two_f,), dev)
+        bias_ptr = bias.data_ptr()
+    codes, scales = _outputs(dev, rows, f, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_swiglu_packed_nvfp4(o.data_ptr(), ld, bias_ptr, rows, f, gsf.data_ptr(),
+                                               codes.data_ptr(), scales.data_ptr(), _stream(stream, dev))
+    _check("h3q_swiglu_packed_nvfp4", rc)
     return codes, scales

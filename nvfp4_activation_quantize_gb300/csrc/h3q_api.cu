@@ -401,6 +401,30 @@ int h3q_quantize_nvfp4_dynamic(const void* x, int64_t ld_x, int64_t rows, int64_
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_swiglu_packed_nvfp4(const void* o, int64_t ld_o, const void* bias, int64_t rows,
+                            int64_t f, const float* global_scale, uint8_t* codes, uint8_t* scales,
+                            void* stream) {
+  static const char* fn = "h3q_swiglu_packed_nvfp4";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, f)) return e;
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "o", o, ld_o, rows, 2 * f)) return e;
+  if (bias != nullptr)
+    if (int e = check_input(fn, "bias", bias, 2 * f, 1, 2 * f)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  const Span in = span(o, view_bytes(rows, 2 * f, ld_o));
+  const Span b = bias ? span(bias, 4 * f) : Span{0, 0};
+  const Span c = span(codes, h3q_code_bytes(rows, f));
+  const Span s = span(scales, h3q_scale_bytes(rows, f));
+  if (overlap(in, c) || overlap(in, s) || overlap(b, c) || overlap(b, s) || overlap(c, s))
+    return invalid(fn, "outputs overlap an input or each other");
+  cudaError_t err = h3q::launch_swiglu_packed(static_cast<const uint16_t*>(o), ld_o,
+                                              static_cast<const uint16_t*>(bias), rows, f,
+                                              global_scale, codes, scales,
+                                              static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
                          const float* global_scale, float* out, void* stream) {
   static const char* fn = "h3q_dequantize_nvfp4";

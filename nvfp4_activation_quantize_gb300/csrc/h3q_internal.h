@@ -58,6 +58,12 @@ cudaError_t launch_residual_adaln(float* h, int64_t ld_h, const uint16_t* o, int
                                   int64_t rows, int64_t cols, const float* gsf, uint8_t* codes,
                                   uint8_t* scales, float* row_rstd, cudaStream_t stream);
 
+// SwiGLU of a value-first packed projection o [rows, 2f] (value o[:, :f], gate
+// o[:, f:]) with its bias [2f] (or NULL) not yet added.
+cudaError_t launch_swiglu_packed(const uint16_t* o, int64_t ld_o, const uint16_t* bias, int64_t rows,
+                                 int64_t f, const float* gsf, uint8_t* codes, uint8_t* scales,
+                                 cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream);
 

@@ -183,13 +183,22 @@ __device__ __forceinline__ void fill_silu_table(float* table) {
   }
 }
 
+// x = bf16(fl(x + b)) for the 16 bf16 values of a block and their biases b.
+__device__ __forceinline__ void add_bias(Block16& x, const Block16& b) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x.w[i] = float2_to_bf16x2(add_bf16x2_f32(b.w[i], bf16x2_to_float2(x.w[i])));
+}
+
 // AMAX: the abs-max pass -- y is formed the same way, its max |y| folded into
-// *amax, and nothing is quantized or stored.
-template <bool AMAX>
+// *amax, and nothing is quantized or stored.  BIAS: gate and up get their
+// per-column biases (bias_gate, bias_up) added and are rounded to bf16 first
+// (the value-first packed projection with its bias not yet added).
+template <bool AMAX, bool BIAS>
 __global__ void __launch_bounds__(kThreads)
 swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
               int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
-              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ amax) {
+              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ amax,
+              const uint16_t* __restrict__ bias_gate, const uint16_t* __restrict__ bias_up) {
   __shared__ float inv_table[128];
   __shared__ __align__(16) float silu_table[2 * kTabHalf];
   const float gsf = AMAX ? 0.0f : *gsf_ptr;
@@ -219,12 +228,17 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
 
   while (row[0] < prows) {
     Block16 gb[kUnroll], ub[kUnroll];
+    Block16 bg[BIAS ? kUnroll : 1], bu[BIAS ? kUnroll : 1];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t g = seg[u] * 32 + lane;
       if (row[u] < rows && g < groups) {
         load_stream(gate + row[u] * ld_gate + g * kBlock, gb[u]);
         load_stream(up + row[u] * ld_up + g * kBlock, ub[u]);
+        if (BIAS) {
+          load_reused(bias_gate + g * kBlock, bg[BIAS ? u : 0]);
+          load_reused(bias_up + g * kBlock, bu[BIAS ? u : 0]);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) gb[u].w[i] = ub[u].w[i] = 0;
@@ -236,6 +250,10 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       const int64_t g = seg[u] * 32 + lane;
       const bool in_row = row[u] < rows;
       const bool in_cols = g < groups;
+      if (BIAS && in_row && in_cols) {
+        add_bias(gb[u], bg[BIAS ? u : 0]);
+        add_bias(ub[u], bu[BIAS ? u : 0]);
+      }
       Block16 y;
       if (__all_sync(0xffffffffu, in_table(gb[u]))) {
         swiglu_block_table(gb[u], ub[u], y, table);
@@ -275,11 +293,28 @@ cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t*
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false>), kThreads,
-                                      0, (work + kWarps - 1) / kWarps, &blocks);
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false, false>),
+                                      kThreads, 0, (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
-  swiglu_kernel<false><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf,
-                                                        codes, scales, nullptr);
+  swiglu_kernel<false, false><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols,
+                                                               gsf, codes, scales, nullptr, nullptr,
+                                                               nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_packed(const uint16_t* o, int64_t ld_o, const uint16_t* bias, int64_t rows,
+                                 int64_t f, const float* gsf, uint8_t* codes, uint8_t* scales,
+                                 cudaStream_t stream) {
+  if (bias == nullptr) return launch_swiglu(o + f, ld_o, o, ld_o, rows, f, gsf, codes, scales, stream);
+  const int64_t segs = (f / 16 + 31) / 32;
+  const int64_t work = (rows + 127) / 128 * 128 * segs;
+  int blocks = 0;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false, true>),
+                                      kThreads, 0, (work + kWarps - 1) / kWarps, &blocks);
+  if (err != cudaSuccess) return err;
+  // value first: up = o[:, :f] with bias[:f], gate = o[:, f:] with bias[f:]
+  swiglu_kernel<false, true><<<blocks, kThreads, 0, stream>>>(o + f, ld_o, o, ld_o, rows, f, gsf,
+                                                              codes, scales, nullptr, bias + f, bias);
   return cudaGetLastError();
 }
 
@@ -293,11 +328,12 @@ cudaError_t launch_swiglu_amax(const uint16_t* gate, int64_t ld_gate, const uint
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = rows * segs;  // no padding rows to visit
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<true>), kThreads,
-                                      0, (work + kWarps - 1) / kWarps, &blocks);
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<true, false>),
+                                      kThreads, 0, (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
-  swiglu_kernel<true><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols, nullptr,
-                                                       nullptr, nullptr, amax);
+  swiglu_kernel<true, false><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols,
+                                                              nullptr, nullptr, nullptr, amax, nullptr,
+                                                              nullptr);
   return cudaGetLastError();
 }
 

@@ -176,3 +176,14 @@ def test_residual_fold_rejects_bad_arguments_on_the_host(lib):
     assert call(o=0x1000000 + 512) == 1 and "overlap" in h3q.h3q_last_error()   # o inside h
     assert call(codes=0x1000000 + 4096) == 1                                     # codes inside h
     assert call(rows=0, h=None, o=None) == h3q.H3Q_OK
+
+
+def test_swiglu_packed_rejects_bad_arguments_on_the_host(lib):
+    # (o, ld_o, bias, rows, f, gsf, codes, scales, stream)
+    f = lib.h3q_swiglu_packed_nvfp4
+    assert f(0x1000000, 512, None, 8, 256, 0x4000000, 0x5000000, 0x6000000, None) in (0, 2)
+    assert f(0x1000000, 500, None, 8, 256, 0x4000000, 0x5000000, 0x6000000, None) == 1  # ld < 2F
+    assert f(0x1000000, 512, 0x2000010, 8, 256, 0x4000000, 0x5000000, 0x6000000, None) == 1
+    assert f(0x1000000, 512, None, 8, 100, 0x4000000, 0x5000000, 0x6000000, None) == 1   # F % 64
+    assert f(0x1000000, 512, None, 8, 256, 0x4000000, 0x1000100, 0x6000000, None) == 1   # codes in o
+    assert f(None, 512, None, 0, 256, None, None, None, None) == h3q.H3Q_OK
