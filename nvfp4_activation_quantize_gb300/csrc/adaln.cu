@@ -506,6 +506,26 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
                                            uint8_t* const (&codes_at)[R],
                                            uint8_t* const (&scale_at)[R], float gsf,
                                            const float* inv_table, float& run_max) {
+  if (AMAX) {
+    // bf16 rounding is monotone in the magnitude, so max |bf16(o)| = bf16(max |o|):
+    // the unrounded values' maximum is rounded once per block
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const float2 rstd2 = make_float2(rstd[k], rstd[k]);
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const ChunkTables& t = tb[i >> 2];
+        const float2 n = mul2(bf16x2_to_float2(v[k][i]), rstd2);
+        const float2 h = mul2(n, t.gm[i & 3]);
+        const float2 m = mul2(h, t.fc[i & 3]);
+        const float2 o = add_bf16x2_f32(t.sh[i & 3], m);
+        am = fmaxf(am, fmaxf(fabsf(o.x), fabsf(o.y)));
+      }
+      run_max = fmaxf(run_max, fabsf(bf16_round(am)));
+    }
+    return;
+  }
   float2 y[R][8];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
@@ -525,10 +545,6 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(y[k][i].x), fabsf(y[k][i].y)));
-    if (AMAX) {  // abs-max pass: no quantize, no store
-      run_max = fmaxf(run_max, amax);
-      continue;
-    }
     const uint32_t sf = block_scale(amax, gsf);
     const float inv = inv_table[sf];
     const float2 inv2 = make_float2(inv, inv);

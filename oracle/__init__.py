@@ -69,6 +69,7 @@ _SIGNATURES = {
     "orc_global_scale": ([_F], _F),
     "orc_amax_bf16": ([_P, _I64], _F),
     "orc_row_rstd_f32": ([_P, _I64, _F], _F),
+    "orc_qkv_epilogue_rows": ([_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _I64, _F, _P], None),
     "orc_swiglu_packed_rows": ([_P, _I64, _P, _I64, _I64, _F, _P, _P, _P, _P], None),
     "orc_residual_adaln_rows": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P], None),
     "orc_global_scale_from_amax": ([_F], _F),
@@ -407,6 +408,32 @@ def swiglu_packed_rows(o_bits, bias_bits, gsf: float | None, want_y: bool = Fals
 
     _run(work, n, threads)
     return codes, sf, y
+
+
+def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: float, is_v: bool,
+                      threads: int = 1) -> np.ndarray:
+    """QKV epilogue of one projected tensor x [n, heads * HD] (bf16 bits) with its bias
+    [heads * HD]: v gets the bias only; q and k the bias, the per-head RMSNorm and the
+    rotate-half RoPE on the first ROT values of each head (cos, sin bf16 [n, ROT]).
+    Returns bf16 bits [n, heads, HD]."""
+    x = _u16(x_bits)
+    n, d = x.shape
+    hd = d // heads
+    assert hd * heads == d and hd % 16 == 0 and hd <= 1024
+    bias = _u16(bias_bits).reshape(d)
+    cos = _u16(cos_bits) if cos_bits is not None else np.zeros((n, 16), np.uint16)
+    sin = _u16(sin_bits) if sin_bits is not None else np.zeros((n, 16), np.uint16)
+    rot = cos.shape[1]
+    assert cos.shape == (n, rot) and sin.shape == (n, rot) and rot <= hd and rot % 2 == 0
+    out = np.empty((n, heads, hd), np.uint16)
+
+    def work(span):
+        a, b = span
+        lib().orc_qkv_epilogue_rows(_ptr(x[a:b]), d, _ptr(bias), b - a, heads, hd, int(is_v),
+                                    _ptr(cos[a:b]), _ptr(sin[a:b]), rot, float(eps), _ptr(out[a:b]))
+
+    _run(work, n, threads)
+    return out
 
 
 def dequantize_rows(codes: np.ndarray, sf_logical: np.ndarray, gsf: float,

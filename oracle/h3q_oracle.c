@@ -488,6 +488,79 @@ void orc_swiglu_packed_rows(const uint16_t *o, int64_t ld_o, const uint16_t *bia
 }
 
 /* ------------------------------------------------------------------------ */
+/* QKV epilogue: bias + per-head RMSNorm + partial RoPE (NEXT row f4)         */
+/* ------------------------------------------------------------------------ */
+/*
+ * [FV-API] qkv_epilogue: projected q/k/v [M, H*HD] bf16 with the bias not yet
+ * added -> roped q, k and biased v, each [M, H, HD]; cos/sin are bf16 [M, ROT]
+ * (the eager path's cos.to(query.dtype)).  [FV-LOG] names the kernel a q/k
+ * norm with partial RoPE.  Readings (the pages print only the wrapper):
+ *   x' = bf16(fl(x + b))                       every tensor (v stops here)
+ *   per head of q and k: rstd over the HD values of x' in the canonical order
+ *   with HD/8 lanes (chunk c of the head on lane c, eight fmaf partials, the
+ *   lane total, a butterfly over the lanes), rstd = fl(1/fl(sqrt(fl(fl(ss/HD)
+ *   + eps)))), no weight (the wrapper takes none), n = bf16(fl(x' * rstd));
+ *   rotate-half RoPE on the first ROT values of each head, each bf16 op of the
+ *   eager path rounded to bf16:
+ *     r_i = -n_{i+ROT/2} (i < ROT/2), n_{i-ROT/2} (ROT/2 <= i < ROT)
+ *     out_i = bf16(fl(bf16(fl(n_i * cos_i)) + bf16(fl(r_i * sin_i))))   i < ROT
+ *     out_i = n_i                                                         i >= ROT
+ */
+static float head_rstd(const float *v, int64_t hd, float eps)
+{
+    int64_t lanes = hd / 8;
+    float lane[128];
+    for (int64_t l = 0; l < lanes; ++l) {
+        float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int e = 0; e < 8; ++e)
+            p[e] = fmaf(v[8 * l + e], v[8 * l + e], p[e]);
+        lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+    }
+    for (int64_t o = lanes / 2; o >= 1; o /= 2) {
+        float next[128];
+        for (int64_t l = 0; l < lanes; ++l)
+            next[l] = lane[l] + lane[l ^ o];
+        memcpy(lane, next, sizeof(float) * (size_t)lanes);
+    }
+    float mean = lane[0] / (float)hd;
+    return 1.0f / sqrtf(mean + eps);
+}
+
+void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias, int64_t nrows,
+                           int64_t heads, int64_t hd, int is_v, const uint16_t *cos_t,
+                           const uint16_t *sin_t, int64_t rot, float eps, uint16_t *out)
+{
+    float xb[1024], n[1024];
+    for (int64_t r = 0; r < nrows; ++r) {
+        for (int64_t hh = 0; hh < heads; ++hh) {
+            const uint16_t *xh = x + r * ld_x + hh * hd;
+            const uint16_t *bh = bias + hh * hd;
+            uint16_t *oh = out + (r * heads + hh) * hd;
+            for (int64_t i = 0; i < hd; ++i)
+                xb[i] = orc_bf16_round(orc_bf16_value(xh[i]) + orc_bf16_value(bh[i]));
+            if (is_v) {
+                for (int64_t i = 0; i < hd; ++i)
+                    oh[i] = orc_bf16_bits(xb[i]);
+                continue;
+            }
+            float rstd = head_rstd(xb, hd, eps);
+            for (int64_t i = 0; i < hd; ++i)
+                n[i] = orc_bf16_round(xb[i] * rstd);
+            for (int64_t i = 0; i < hd; ++i) {
+                if (i >= rot) {
+                    oh[i] = orc_bf16_bits(n[i]);
+                    continue;
+                }
+                float rr = i < rot / 2 ? -n[i + rot / 2] : n[i - rot / 2];
+                float a = orc_bf16_round(n[i] * orc_bf16_value(cos_t[r * rot + i]));
+                float b = orc_bf16_round(rr * orc_bf16_value(sin_t[r * rot + i]));
+                oh[i] = orc_bf16_bits(a + b);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Residual fold + RMSNorm + AdaLN (NEXT row f1)                              */
 /* ------------------------------------------------------------------------ */
 /*
