@@ -421,8 +421,9 @@ def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: fl
     hd = d // heads
     assert hd * heads == d and hd % 16 == 0 and hd <= 1024
     bias = _u16(bias_bits).reshape(d)
-    cos = _u16(cos_bits) if cos_bits is not None else np.zeros((n, 16), np.uint16)
-    sin = _u16(sin_bits) if sin_bits is not None else np.zeros((n, 16), np.uint16)
+    # ROT is the tables' width; no tables is ROT = 0: the norm without a rotation
+    cos = _u16(cos_bits) if cos_bits is not None else np.zeros((n, 0), np.uint16)
+    sin = _u16(sin_bits) if sin_bits is not None else np.zeros((n, 0), np.uint16)
     rot = cos.shape[1]
     assert cos.shape == (n, rot) and sin.shape == (n, rot) and rot <= hd and rot % 2 == 0
     out = np.empty((n, heads, hd), np.uint16)

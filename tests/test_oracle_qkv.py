@@ -80,3 +80,12 @@ def test_rotate_half_rope_op_by_op(rot):
     want = _r(_r(first * c) + _r(rotated * s))
     assert np.array_equal(out[..., :rot].view(np.uint32), want.view(np.uint32))
     assert np.array_equal(out[..., rot:].view(np.uint32), nrm[..., rot:].view(np.uint32))
+
+
+def test_no_tables_is_the_norm_without_a_rotation():
+    """ROT = 0 (no cos/sin tables) leaves every normed value as it is: the same as
+    ROT = 16 with cos = 1 and sin = 0 (n * 1 + r * 0 = n exactly)."""
+    n, heads = 7, 3
+    x, b, _, _ = _inputs(n, heads, 64, 12)
+    got = oracle.qkv_epilogue_rows(x, b, heads, None, None, 1e-6, is_v=False)
+    assert np.array_equal(got, _normed(x, b, heads, n))
