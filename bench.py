@@ -80,6 +80,12 @@ def residual_bytes(rows: int, cols: int, frames: int) -> int:
     return (4 + 4 + 2) * rows * cols + out_bytes(rows, cols) + 2 * 2 * cols + frames * 3 * cols * 2 + 4
 
 
+def qkv_bytes(rows: int, heads: int, head_dim: int, rot: int) -> int:
+    # q, k, v read and written (bf16), their biases, the cos and sin tables
+    d = heads * head_dim
+    return 3 * 2 * rows * d * 2 + 3 * d * 2 + 2 * rows * rot * 2
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -482,6 +488,23 @@ def measure_producers(h3q, dev, stream, args):
     res["residual_adaln_65280x7168"] = entry(residual_bytes(ROWS, COLS, FRAMES), per, ROWS)
     del w, c, s
 
+    # QKV epilogue: 65,280 tokens x 56 heads x 128 (ROT 64), q, k, v column slices of
+    # one packed projection, bf16 [rows, heads, 128] outputs
+    w = workloads.qkv_inputs(dev)
+    outs = h3q.h3q_qkv_epilogue(w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"],
+                                w["eps"], stream=stream)
+
+    def qkv_step():
+        h3q.h3q_qkv_epilogue(w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"],
+                             w["eps"], outs=outs, stream=stream)
+
+    for _ in range(3):
+        qkv_step()
+    _, per = time_launches(qkv_step, n, stream)
+    res["qkv_epilogue_65280x56x128_rot64"] = entry(qkv_bytes(ROWS, w["heads"], w["head_dim"], w["rot"]),
+                                                   per, ROWS)
+    del w, outs
+
     # standalone quantize 8,192 x 7,168 (150 MB: near L2, so L2 is flushed before each launch)
     x = workloads.quantize_inputs(dev)
     g = torch.tensor([2688.0 / float(x.float().abs().max())], dtype=torch.float32, device=dev)
@@ -605,6 +628,15 @@ def run_single(args, dev):
             w["h"], w["o"], w["gate"], w["gamma"], w["table"], g, bias=w["bias"], rows_per_frame=RPF,
             eps=w["eps"], codes=c, scales=s, stream=stream)
         nbytes = residual_bytes(rows, COLS, w["table"].shape[0])
+    elif kind == "qkv":
+        rows = args.rows or ROWS
+        w = workloads.qkv_inputs(dev, rows=rows)
+        outs = h3q.h3q_qkv_epilogue(w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"],
+                                    w["heads"], w["eps"], stream=stream)
+        fn = lambda: h3q.h3q_qkv_epilogue(  # noqa: E731
+            w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"], w["eps"], outs=outs,
+            stream=stream)
+        nbytes = qkv_bytes(rows, w["heads"], w["head_dim"], w["rot"])
     else:
         rows = args.rows or ROWS
         x = workloads.attention_output(dev, tokens=rows)
@@ -637,7 +669,7 @@ def main(argv=None):
     p.add_argument("--reference-rows", type=int, default=510)
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize", "residual"],
+    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize", "residual", "qkv"],
                    help="time one producer alone (for profiling); prints a short JSON line")
     p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)

@@ -282,6 +282,42 @@ int h3q_quantize_nvfp4_dynamic(const void *x, int64_t ld_x, int64_t rows, int64_
                                float *global_scale, uint8_t *codes, uint8_t *scales,
                                void *stream);
 
+/*
+ * QKV epilogue: bias + per-head RMSNorm + partial rotate-half RoPE on q and k,
+ * bias only on v (the step after the QKV projection GEMM; bf16 out, no
+ * quantize).  FastVideo API page, qkv_epilogue: projected q/k/v [M, H*HD] bf16
+ * with the bias not yet added -> roped q, k and biased v, each [M, H, HD];
+ * cos/sin bf16 [M, ROT] (the eager path's cos.to(query.dtype)); an eps and no
+ * norm weights.  FastVideo commit log (the q/k norm + partial RoPE kernel):
+ * offsets are 64-bit, so M * H * HD may exceed 2^31.  Per row and head, with
+ * x' = bf16(fl(x + b)) for each of the HD values:
+ *   v:     out = x'
+ *   q, k:  ss = the head's sum of squares of x' (eight fmaf partials per chunk
+ *          of 8 values, the chunk total ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)),
+ *          a butterfly over the head's HD/8 chunk totals);
+ *          rstd = fl(1 / fl(sqrt(fl(fl(ss / HD) + eps)))), n = bf16(fl(x' * rstd));
+ *          out_i = bf16(fl(bf16(fl(n_i * cos_i)) + bf16(fl(r_i * sin_i)))) for
+ *          i < ROT, r_i = -n_{i+ROT/2} (i < ROT/2) or n_{i-ROT/2}; out_i = n_i
+ *          for i >= ROT.
+ *
+ *   q, k, v        bf16 [rows, heads * head_dim], row strides ld_q, ld_k, ld_v
+ *                  (>= heads * head_dim, multiples of 16), 32-byte aligned.
+ *   bias_q/k/v     bf16 [heads * head_dim], 32-byte aligned, not NULL.
+ *   cos, sin       bf16 [rows, rot] contiguous, 16-byte aligned; NULL when rot = 0.
+ *   rot            ROT, a multiple of 16 with 0 <= rot <= head_dim.
+ *   heads          H >= 1; head_dim HD in {64, 128, 256}; heads * head_dim <= 2^24.
+ *   eps            finite, >= 0.
+ *   q_out, k_out, v_out  bf16 [rows, heads, head_dim] contiguous, 16-byte
+ *                  aligned, caller-owned; they must not overlap an input or
+ *                  each other.
+ * rows = 0 returns H3Q_OK with no launch.  Status codes as the other calls.
+ */
+int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, const void *v,
+                     int64_t ld_v, const void *bias_q, const void *bias_k, const void *bias_v,
+                     const void *cos, const void *sin, int64_t rot, int64_t rows, int64_t heads,
+                     int64_t head_dim, float eps, void *q_out, void *k_out, void *v_out,
+                     void *stream);
+
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char *h3q_last_error(void);
 

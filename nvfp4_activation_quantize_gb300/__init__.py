@@ -24,6 +24,7 @@ __all__ = [
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
     "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
+    "h3q_qkv_epilogue",
 ]
 
 H3Q_OK = 0
@@ -46,6 +47,8 @@ _SIGNATURES = {
     "h3q_swiglu_packed_nvfp4": [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P],
     "h3q_residual_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _I64,
                                          ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P],
+    "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                         ctypes.c_float, _P, _P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -449,3 +452,39 @@ def h3q_swiglu_packed_nvfp4(o, global_scale, bias=None, codes=None, scales=None,
                                                codes.data_ptr(), scales.data_ptr(), _stream(stream, dev))
     _check("h3q_swiglu_packed_nvfp4", rc)
     return codes, scales
+
+
+def h3q_qkv_epilogue(q, k, v, biases, cos, sin, heads, eps, outs=None, stream=None):
+    """QKV epilogue of projected q, k, v [rows, heads * HD] bf16 (bias not yet added):
+    returns (q_out, k_out, v_out), each bf16 [rows, heads, HD], with q and k biased,
+    RMS-normed per head and rotated (rotate-half RoPE on each head's first ROT
+    values, cos and sin bf16 [rows, ROT]; None for ROT = 0) and v biased."""
+    import torch
+
+    q, rows, d, ld_q = _rows_view("q", q, torch.bfloat16)
+    dev = q.device
+    k, rows_k, d_k, ld_k = _rows_view("k", k, torch.bfloat16, dev)
+    v, rows_v, d_v, ld_v = _rows_view("v", v, torch.bfloat16, dev)
+    if (rows_k, d_k) != (rows, d) or (rows_v, d_v) != (rows, d):
+        raise ValueError("q, k and v must have the same shape")
+    if heads < 1 or d % heads:
+        raise ValueError("the columns of q must split into heads")
+    hd = d // heads
+    b = [_contiguous(n, t, torch.bfloat16, (d,), dev) for n, t in zip(("bias_q", "bias_k", "bias_v"), biases)]
+    rot, cos_ptr, sin_ptr = 0, None, None
+    if cos is not None or sin is not None:
+        rot = cos.shape[-1] if cos.dim() == 2 else -1
+        _contiguous("cos", cos, torch.bfloat16, (rows, rot), dev)
+        _contiguous("sin", sin, torch.bfloat16, (rows, rot), dev)
+        cos_ptr, sin_ptr = cos.data_ptr(), sin.data_ptr()
+    if outs is None:
+        outs = [torch.empty((rows, heads, hd), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    outs = [_contiguous(n, t, torch.bfloat16, (rows, heads, hd), dev)
+            for n, t in zip(("q_out", "k_out", "v_out"), outs)]
+    with torch.cuda.device(dev):
+        rc = library().h3q_qkv_epilogue(q.data_ptr(), ld_q, k.data_ptr(), ld_k, v.data_ptr(), ld_v,
+                                        b[0].data_ptr(), b[1].data_ptr(), b[2].data_ptr(), cos_ptr,
+                                        sin_ptr, rot, rows, heads, hd, float(eps), outs[0].data_ptr(),
+                                        outs[1].data_ptr(), outs[2].data_ptr(), _stream(stream, dev))
+    _check("h3q_qkv_epilogue", rc)
+    return outs[0], outs[1], outs[2]

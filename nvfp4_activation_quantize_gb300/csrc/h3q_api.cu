@@ -446,4 +446,70 @@ int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t ro
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_qkv_epilogue(const void* q, int64_t ld_q, const void* k, int64_t ld_k, const void* v,
+                     int64_t ld_v, const void* bias_q, const void* bias_k, const void* bias_v,
+                     const void* cos, const void* sin, int64_t rot, int64_t rows, int64_t heads,
+                     int64_t head_dim, float eps, void* q_out, void* k_out, void* v_out,
+                     void* stream) {
+  static const char* fn = "h3q_qkv_epilogue";
+  g_last_error.clear();
+  if (rows < 0) return invalid(fn, "rows must be >= 0");
+  if (rows > kMaxRows) return invalid(fn, "rows exceeds 2^40");
+  if (heads < 1) return invalid(fn, "heads must be >= 1");
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return invalid(fn, "head_dim must be 64, 128 or 256");
+  if (heads > kMaxCols / head_dim) return invalid(fn, "heads * head_dim exceeds 2^24");
+  if (rot < 0 || rot > head_dim || rot % 16 != 0)
+    return invalid(fn, "rot must be a multiple of 16 in [0, head_dim]");
+  if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
+  if (rows == 0) return H3Q_OK;
+  const int64_t d = heads * head_dim;
+  const void* xs[3] = {q, k, v};
+  const int64_t lds[3] = {ld_q, ld_k, ld_v};
+  const void* bs[3] = {bias_q, bias_k, bias_v};
+  void* outs[3] = {q_out, k_out, v_out};
+  static const char* xn[3] = {"q", "k", "v"};
+  static const char* bn[3] = {"bias_q", "bias_k", "bias_v"};
+  for (int i = 0; i < 3; ++i) {
+    if (int e = check_input(fn, xn[i], xs[i], lds[i], rows, d)) return e;
+    if (int e = check_input(fn, bn[i], bs[i], d, 1, d)) return e;
+    if (outs[i] == nullptr || !aligned(outs[i], 16))
+      return invalid(fn, "q_out, k_out and v_out must be 16-byte aligned and not NULL");
+  }
+  if (rot > 0) {
+    if (cos == nullptr || sin == nullptr) return invalid(fn, "cos and sin must not be NULL when rot > 0");
+    if (!aligned(cos, 16) || !aligned(sin, 16)) return invalid(fn, "cos and sin must be 16-byte aligned");
+  }
+  Span ins[8];
+  int n_in = 0;
+  for (int i = 0; i < 3; ++i) {
+    ins[n_in++] = span(xs[i], view_bytes(rows, d, lds[i]));
+    ins[n_in++] = span(bs[i], d * 2);
+  }
+  if (rot > 0) {
+    ins[n_in++] = span(cos, rows * rot * 2);
+    ins[n_in++] = span(sin, rows * rot * 2);
+  }
+  Span os[3];
+  for (int i = 0; i < 3; ++i) os[i] = span(outs[i], rows * d * 2);
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (overlap(os[i], ins[j])) return invalid(fn, "outputs overlap an input or each other");
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(os[i], os[j])) return invalid(fn, "outputs overlap an input or each other");
+  }
+  const uint16_t* x16[3];
+  const uint16_t* b16[3];
+  uint16_t* o16[3];
+  for (int i = 0; i < 3; ++i) {
+    x16[i] = static_cast<const uint16_t*>(xs[i]);
+    b16[i] = static_cast<const uint16_t*>(bs[i]);
+    o16[i] = static_cast<uint16_t*>(outs[i]);
+  }
+  cudaError_t err = h3q::launch_qkv_epilogue(
+      x16, lds, b16, o16, static_cast<const uint16_t*>(cos), static_cast<const uint16_t*>(sin), rot,
+      rows, heads, head_dim, eps, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 }  // extern "C"

@@ -187,3 +187,45 @@ def test_swiglu_packed_rejects_bad_arguments_on_the_host(lib):
     assert f(0x1000000, 512, None, 8, 100, 0x4000000, 0x5000000, 0x6000000, None) == 1   # F % 64
     assert f(0x1000000, 512, None, 8, 256, 0x4000000, 0x1000100, 0x6000000, None) == 1   # codes in o
     assert f(None, 512, None, 0, 256, None, None, None, None) == h3q.H3Q_OK
+
+
+def test_qkv_epilogue_rejects_bad_arguments_on_the_host(lib):
+    # (q, ld_q, k, ld_k, v, ld_v, bias_q, bias_k, bias_v, cos, sin, rot, rows, heads, head_dim,
+    #  eps, q_out, k_out, v_out, stream): 8 rows of 2 heads of 128
+    names = ["q", "ld_q", "k", "ld_k", "v", "ld_v", "bq", "bk", "bv", "cos", "sin", "rot", "rows",
+             "heads", "hd", "eps", "qo", "ko", "vo", "stream"]
+    good = [0x1000000, 256, 0x1100000, 256, 0x1200000, 256, 0x2000000, 0x2100000, 0x2200000,
+            0x3000000, 0x3100000, 64, 8, 2, 128, 1e-6, 0x4000000, 0x4100000, 0x4200000, None]
+    f = lib.h3q_qkv_epilogue
+
+    def call(**kw):
+        a = list(good)
+        for name, value in kw.items():
+            a[names.index(name)] = value
+        return f(*a)
+
+    assert call() in (0, 2)
+    assert call(hd=96, ld_q=192, ld_k=192, ld_v=192) == 1 and "head_dim" in h3q.h3q_last_error()
+    assert call(rot=24) == 1 and "rot" in h3q.h3q_last_error()
+    assert call(rot=144) == 1                                          # rot > head_dim
+    assert call(heads=0) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(ld_k=200) == 1                                          # ld < H * HD
+    assert call(k=0x1100010) == 1                                       # k not 32-byte aligned
+    assert call(bv=None) == 1
+    assert call(cos=None) == 1 and "cos" in h3q.h3q_last_error()
+    assert call(rot=0, cos=None, sin=None) in (0, 2)                    # no rotation, no tables
+    assert call(sin=0x3100008) == 1                                     # sin not 16-byte aligned
+    assert call(vo=0x1000000 + 256) == 1 and "overlap" in h3q.h3q_last_error()  # v_out inside q
+    assert call(ko=0x4000000 + 4096 - 16) == 1 and "overlap" in h3q.h3q_last_error()  # k_out on q_out
+    assert call(qo=0x3000000) == 1                                      # q_out on cos
+    assert call(rows=0, q=None, k=None, v=None) == h3q.H3Q_OK
+
+
+def test_python_binding_of_the_qkv_epilogue_refuses_host_tensors():
+    import torch
+
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    b = torch.zeros(256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        h3q.h3q_qkv_epilogue(x, x, x, (b, b, b), None, None, 2, 1e-6)

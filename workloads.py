@@ -149,6 +149,35 @@ def attention_output(device, tokens: int = ATTN_TOKENS, heads: int = 56, head_di
     return _normal_bf16(tokens, heads * head_dim, gen, device)
 
 
+def qkv_inputs(device, rows: int = TOKENS, heads: int = 56, head_dim: int = 128, rot: int = 64,
+               seed: int = 7, packed: bool = True) -> dict:
+    """QKV epilogue inputs: the projection output [rows, 3 * heads * head_dim] bf16 ~
+    N(0, 1) * s_j with per-channel s_j ~ LogNormal(0, 0.5) (q, k and v are its three
+    column slices when `packed`, else three contiguous tensors of the same values),
+    biases [heads * head_dim] ~ N(0, 0.1), and cos/sin [rows, rot] bf16 of an angle
+    theta ~ U(0, 2 pi) per row and pair, the pair's two halves sharing the angle
+    (the rotate-half table layout); eps 1e-6."""
+    import math
+
+    gen = _gen(device, seed)
+    d = heads * head_dim
+    col_scale = torch.exp(0.5 * torch.randn(3 * d, generator=gen, device=device, dtype=torch.float32))
+    proj = _normal_bf16(rows, 3 * d, gen, device, col_scale=col_scale)
+    if packed:
+        q, k, v = proj[:, :d], proj[:, d:2 * d], proj[:, 2 * d:]
+    else:
+        q, k, v = (proj[:, i * d:(i + 1) * d].contiguous() for i in range(3))
+        del proj
+    biases = tuple(_normal_bf16(1, d, gen, device, std=0.1).reshape(d) for _ in range(3))
+    cos = sin = None
+    if rot:
+        theta = torch.rand((rows, rot // 2), generator=gen, device=device) * (2 * math.pi)
+        cos = torch.cat([theta.cos(), theta.cos()], 1).to(torch.bfloat16)
+        sin = torch.cat([theta.sin(), theta.sin()], 1).to(torch.bfloat16)
+    return {"q": q, "k": k, "v": v, "biases": biases, "cos": cos, "sin": sin, "heads": heads,
+            "head_dim": head_dim, "rot": rot, "eps": 1e-6}
+
+
 def sample_rows(rows: int, head: int = 256, tail: int = 256, random: int = 4096,
                 seed: int = 0) -> torch.Tensor:
     """Row indices for sampled checks on full-size outputs: the first `head`, the
