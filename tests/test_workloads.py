@@ -35,3 +35,17 @@ def test_sample_rows():
     s = workloads.sample_rows(1000, head=10, tail=10, random=50)
     assert s[0] == 0 and s[-1] == 999 and len(set(s.tolist())) == len(s)
     assert workloads.sample_rows(5).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_qkv_inputs_layout():
+    w = workloads.qkv_inputs("cpu", rows=9, heads=3, head_dim=64, rot=32)
+    assert w["q"].shape == w["k"].shape == w["v"].shape == (9, 192)
+    assert w["q"].stride(0) == 3 * 192 and w["k"].data_ptr() - w["q"].data_ptr() == 192 * 2
+    assert all(b.shape == (192,) for b in w["biases"])
+    c, s = w["cos"].float(), w["sin"].float()
+    assert c.shape == s.shape == (9, 32)
+    assert torch.equal(c[:, :16], c[:, 16:]) and torch.equal(s[:, :16], s[:, 16:])  # halves share theta
+    assert (c * c + s * s - 1).abs().max() < 0.02
+    u = workloads.qkv_inputs("cpu", rows=9, heads=3, head_dim=64, rot=32, packed=False)
+    assert u["q"].is_contiguous() and torch.equal(u["k"], w["k"])
+    assert workloads.qkv_inputs("cpu", rows=2, heads=1, rot=0)["cos"] is None
