@@ -570,7 +570,11 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
 // the rstd (from the warp totals, one lane per row), the frame and the row's
 // scale offset, and announces them on a named barrier that the other warps wait
 // on before pass 2; the per-row bookkeeping is thus done once per row, not once
-// per thread.
+// per thread.  There is no CTA-wide barrier per step: the other warps announce
+// on a second named barrier that a step's totals are posted (which only the
+// stats warp waits on), and a ring stage is refilled only after the "rows
+// published" barrier of the next step, which every warp reaches after its pass 2
+// of the step that stage held.
 // Per-row values published by the stats warp for one step.
 struct RowInfo {
   float rstd;
@@ -673,14 +677,18 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   uint8_t* const scale_t = a.scales + (t >> 2) * 512 + (t & 3);
   for (int64_t q = 0; q < steps; ++q) {
     if (warp == kStatsWarp) {
+      if (q > 0) named_sync(2, NB);  // step q's totals posted; every warp past barrier 1 of step q-1
       stats(q);
       __syncwarp();
       named_arrive(1, NB);
+      cp_async_commit();  // keep the group count in step with the copying warps
+    } else {
+      cp_async_wait<kStages - 3>();  // step q+1 landed (this thread's copies)
+      pass1(q + 1);
+      named_sync(1, NB);  // rows of step q published; every warp done with step q-1
+      if (q + 1 < steps) named_arrive(2, NB);  // step q+1's totals posted
+      issue();  // step q+3 into step q-1's stage
     }
-    issue();
-    cp_async_wait<kStages - 2>();  // step q+1 landed (this thread's copies)
-    pass1(q + 1);
-    if (warp != kStatsWarp) named_sync(1, NB);  // rows of step q published
 
     const int n = static_cast<int>(r_end - r_begin - R * q < R ? r_end - r_begin - R * q : R);
     const uint4* buf = ring + (q % kStages) * R * kChunks + 2 * t;
@@ -724,7 +732,6 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
       }
     }
     code_step += R * kCodeRow;
-    __syncthreads();  // step q+1's totals and copies; step q's ring stage and rows are free
   }
   cp_async_wait<0>();
   if (AMAX)

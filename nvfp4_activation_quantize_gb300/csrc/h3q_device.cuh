@@ -108,6 +108,19 @@ __device__ __forceinline__ float2 add_bf16x2_f32(uint32_t b, float2 c) {
   return r;
 }
 
+// bf16(a + b) for each half of two bf16 pairs: add.rn.bf16x2 rounds the exact
+// sum once.  That equals bf16(fl(a + b)), the sum formed in binary32 and then
+// rounded to bf16: rounding first to 24 bits and then to 8 cannot differ from
+// rounding once to 8 for the sum of two 8-bit operands, since 24 >= 2 * 8 + 2
+// (S. A. Figueroa, "When is double rounding innocuous?", ACM SIGNUM Newsletter
+// 30(3), 1995).  Checked for every pair of bf16 values by
+// tests/device/identities.cu.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // fl(1 / d) for two d in [1, 2^126): a hardware reciprocal estimate refined by
 // one Newton-Raphson step and Markstein's final correction (P. Markstein,
 // "Computation of elementary functions on the IBM RISC System/6000 processor",

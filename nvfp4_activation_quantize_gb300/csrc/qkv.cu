@@ -69,12 +69,13 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
 // bf16 pair w with its sign bits flipped: the exact negation of both values.
 __device__ __forceinline__ uint32_t neg_bf16x2(uint32_t w) { return w ^ 0x80008000u; }
 
-// x' = bf16(fl(x + b)) for the eight values of a chunk.
+// x' = bf16(fl(x + b)) for the eight values of a chunk (one bf16x2 add per
+// pair: the same bits, see add_bf16x2).
 __device__ __forceinline__ void biased(const uint4& xw, const uint4& bw, uint32_t* xb) {
-  const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
-  const uint32_t bs[4] = {bw.x, bw.y, bw.z, bw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) xb[i] = float2_to_bf16x2(add_bf16x2_f32(bs[i], bf16x2_to_float2(xs[i])));
+  xb[0] = add_bf16x2(xw.x, bw.x);
+  xb[1] = add_bf16x2(xw.y, bw.y);
+  xb[2] = add_bf16x2(xw.z, bw.z);
+  xb[3] = add_bf16x2(xw.w, bw.w);
 }
 
 // One (row, tensor) unit: the row's heads of q, k or v, `kHeadsPerWarp` at a
@@ -147,7 +148,7 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
             const uint32_t r = c < half ? neg_bf16x2(pw[i]) : pw[i];
             const uint32_t p1 = float2_to_bf16x2(mul2(bf16x2_to_float2(nw[i]), bf16x2_to_float2(cs[i])));
             const uint32_t p2 = float2_to_bf16x2(mul2(bf16x2_to_float2(r), bf16x2_to_float2(sn[i])));
-            o[i] = float2_to_bf16x2(add2(bf16x2_to_float2(p1), bf16x2_to_float2(p2)));
+            o[i] = add_bf16x2(p1, p2);  // bf16(fl(p1 + p2)) of two bf16 values
           }
           res = make_uint4(o[0], o[1], o[2], o[3]);
         }

@@ -169,9 +169,9 @@ __device__ __forceinline__ void fold_chunk(float (&hv)[8], const uint4& ov, cons
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    // u as a bf16 pair: o itself, or bf16(fl(o + bias)) rounded by one cvt
-    const uint32_t u = has_bias ? float2_to_bf16x2(add_bf16x2_f32(bw[i], bf16x2_to_float2(ow[i])))
-                                : ow[i];
+    // u as a bf16 pair: o itself, or bf16(fl(o + bias)) by one bf16x2 add (the
+    // same bits, see add_bf16x2)
+    const uint32_t u = has_bias ? add_bf16x2(ow[i], bw[i]) : ow[i];
     const float2 t = mul2(bf16x2_to_float2(u), bf16x2_to_float2(gw[i]));
     // scalar adds: a paired add of a paired product would be contracted
     hv[2 * i] = __fadd_rn(hv[2 * i], t.x);

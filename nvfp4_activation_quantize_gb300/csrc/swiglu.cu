@@ -183,10 +183,11 @@ __device__ __forceinline__ void fill_silu_table(float* table) {
   }
 }
 
-// x = bf16(fl(x + b)) for the 16 bf16 values of a block and their biases b.
+// x = bf16(fl(x + b)) for the 16 bf16 values of a block and their biases b
+// (one bf16x2 add per pair: the same bits, see add_bf16x2).
 __device__ __forceinline__ void add_bias(Block16& x, const Block16& b) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) x.w[i] = float2_to_bf16x2(add_bf16x2_f32(b.w[i], bf16x2_to_float2(x.w[i])));
+  for (int i = 0; i < 8; ++i) x.w[i] = add_bf16x2(x.w[i], b.w[i]);
 }
 
 // AMAX: the abs-max pass -- y is formed the same way, its max |y| folded into
@@ -228,17 +229,12 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
 
   while (row[0] < prows) {
     Block16 gb[kUnroll], ub[kUnroll];
-    Block16 bg[BIAS ? kUnroll : 1], bu[BIAS ? kUnroll : 1];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t g = seg[u] * 32 + lane;
       if (row[u] < rows && g < groups) {
         load_stream(gate + row[u] * ld_gate + g * kBlock, gb[u]);
         load_stream(up + row[u] * ld_up + g * kBlock, ub[u]);
-        if (BIAS) {
-          load_reused(bias_gate + g * kBlock, bg[BIAS ? u : 0]);
-          load_reused(bias_up + g * kBlock, bu[BIAS ? u : 0]);
-        }
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) gb[u].w[i] = ub[u].w[i] = 0;
@@ -251,8 +247,14 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
       const bool in_row = row[u] < rows;
       const bool in_cols = g < groups;
       if (BIAS && in_row && in_cols) {
-        add_bias(gb[u], bg[BIAS ? u : 0]);
-        add_bias(ub[u], bu[BIAS ? u : 0]);
+        // the biases are loaded here rather than with x: they are re-read by
+        // every row and stay in L1, and holding them across the batch would
+        // cost the registers (and so the resident warps) that keep x in flight
+        Block16 b;
+        load_reused(bias_gate + g * kBlock, b);
+        add_bias(gb[u], b);
+        load_reused(bias_up + g * kBlock, b);
+        add_bias(ub[u], b);
       }
       Block16 y;
       if (__all_sync(0xffffffffu, in_table(gb[u]))) {

@@ -1,8 +1,10 @@
 """The kernels' division-free routines against CUDA's correctly rounded operations,
 exhaustively on the GPU: the Markstein reciprocal used for the SiLU sigmoid over
-every binary32 in [1, 2^126), and the once-corrected fl(a/6) of the block scale
-over every bf16 value (tests/device/identities.cu, compiled here with the
-library's own flags)."""
+every binary32 in [1, 2^126), the once-corrected fl(a/6) of the block scale
+over every bf16 value, and the one-instruction bf16 sum (the bias adds and the
+RoPE sum) against the binary32 sum rounded to bf16 over every pair of bf16
+values (tests/device/identities.cu, compiled here with the library's own
+flags)."""
 import os
 import subprocess
 
@@ -25,3 +27,4 @@ def test_division_free_routines_match_cuda(tmp_path):
     res = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stdout + res.stderr
     assert "rcp_rn_ge1 mismatches 0" in res.stdout and "amax_over_six mismatches 0" in res.stdout
+    assert "add_bf16x2 mismatches 0 of 4294967296" in res.stdout
