@@ -421,10 +421,8 @@ def measure_producers(h3q, dev, stream, args):
     del c, s
 
     # SwiGLU of the value-first packed projection with its bias, 65,280 x 2 x 18,944
-    o = torch.empty((ROWS, 2 * workloads.FFN), dtype=torch.bfloat16, device=dev)
-    o[:, :workloads.FFN], o[:, workloads.FFN:] = up, gate
     del gate, up
-    bias = torch.zeros(2 * workloads.FFN, dtype=torch.bfloat16, device=dev).normal_(0.0, 0.2)
+    o, bias = workloads.swiglu_packed_inputs(dev)
     c, s = h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, stream=stream)
     for _ in range(3):
         h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, codes=c, scales=s, stream=stream)
@@ -618,6 +616,15 @@ def run_single(args, dev):
         c, s = h3q.h3q_swiglu_nvfp4(gate, up, g, stream=stream)
         fn = lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)  # noqa: E731
         nbytes = swiglu_bytes(rows, workloads.FFN)
+    elif kind == "swiglu_packed":
+        rows = args.rows or ROWS
+        o, bias = workloads.swiglu_packed_inputs(dev, rows=rows)
+        f = workloads.FFN
+        g = torch.tensor([calibrate_swiglu_gsf(o[:, f:], o[:, :f])], dtype=torch.float32, device=dev)
+        c, s = h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, stream=stream)
+        fn = lambda: h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, codes=c, scales=s,  # noqa: E731
+                                                 stream=stream)
+        nbytes = swiglu_bytes(rows, workloads.FFN) + 4 * workloads.FFN
     elif kind == "residual":
         rows = args.rows or ROWS
         w = workloads.residual_inputs(dev, rows=rows, frames=max(1, -(-rows // RPF)))
@@ -669,7 +676,7 @@ def main(argv=None):
     p.add_argument("--reference-rows", type=int, default=510)
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["adaln", "swiglu", "quantize", "residual", "qkv"],
+    p.add_argument("--kernel", choices=["adaln", "swiglu", "swiglu_packed", "quantize", "residual", "qkv"],
                    help="time one producer alone (for profiling); prints a short JSON line")
     p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)

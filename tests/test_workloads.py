@@ -49,3 +49,11 @@ def test_qkv_inputs_layout():
     u = workloads.qkv_inputs("cpu", rows=9, heads=3, head_dim=64, rot=32, packed=False)
     assert u["q"].is_contiguous() and torch.equal(u["k"], w["k"])
     assert workloads.qkv_inputs("cpu", rows=2, heads=1, rot=0)["cos"] is None
+
+
+def test_swiglu_packed_inputs_are_value_first():
+    gate, up = workloads.swiglu_inputs("cpu", rows=5, cols=64)
+    o, bias = workloads.swiglu_packed_inputs("cpu", rows=5, cols=64)
+    assert o.shape == (5, 128) and bias.shape == (128,)
+    assert torch.equal(o[:, :64], up) and torch.equal(o[:, 64:], gate)
+    assert torch.equal(bias, workloads.swiglu_packed_inputs("cpu", rows=5, cols=64)[1])

@@ -141,6 +141,18 @@ def swiglu_inputs(device, rows: int = TOKENS, cols: int = FFN, seed: int = 4,
     return gate, up
 
 
+def swiglu_packed_inputs(device, rows: int = TOKENS, cols: int = FFN, seed: int = 4, std: float = 1.5,
+                         bias_std: float = 0.2) -> tuple[torch.Tensor, torch.Tensor]:
+    """The value-first packed projection o [rows, 2 * cols] = [up | gate] with the
+    values of swiglu_inputs(seed), and its bias [2 * cols] ~ N(0, bias_std^2)
+    (drawn from seed + 100)."""
+    gate, up = swiglu_inputs(device, rows=rows, cols=cols, seed=seed, std=std)
+    o = torch.cat([up, gate], 1)
+    del gate, up
+    bias = _normal_bf16(1, 2 * cols, _gen(device, seed + 100), device, std=bias_std).reshape(2 * cols)
+    return o, bias
+
+
 def attention_output(device, tokens: int = ATTN_TOKENS, heads: int = 56, head_dim: int = 128,
                      seed: int = 5) -> torch.Tensor:
     """Attention output bf16 [1, tokens, heads, head_dim] ~ N(0, 1), returned as the
