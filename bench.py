@@ -112,10 +112,9 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, path: str | None = None):
-    """DRAM bytes per launch of `kernel` from profiles/dram_traffic.txt, if they were
-    taken from the current kernel sources (lines: kernel source-hash bytes note)."""
-    path = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
+def recorded_value(kernel: str, path: str):
+    """The number recorded for `kernel` in a profiles/ record (lines: kernel
+    source-hash value), if it was taken from the current kernel sources."""
     if not os.path.exists(path):
         return None
     want = kernel_source_hash(kernel)
@@ -123,8 +122,15 @@ def recorded_traffic(kernel: str, path: str | None = None):
         for line in f:
             parts = line.split()
             if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
-                return int(parts[2]) if parts[1] == want else None
+                return float(parts[2]) if parts[1] == want else None
     return None
+
+
+def recorded_traffic(kernel: str, path: str | None = None):
+    """DRAM bytes per launch of `kernel` from profiles/dram_traffic.txt, if they were
+    taken from the current kernel sources (lines: kernel source-hash bytes)."""
+    v = recorded_value(kernel, path or os.path.join(ROOT, "profiles", "dram_traffic.txt"))
+    return None if v is None else int(v)
 
 
 # --------------------------------------------------------------------------- #
@@ -196,6 +202,23 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # timing helpers                                                                #
 # --------------------------------------------------------------------------- #
+
+def memcpy_d2d_ceiling(dev, stream, nbytes: int = 4 << 30, reps: int = 10) -> dict:
+    """A plain device-to-device copy (torch's copy_ of a contiguous buffer, a
+    cudaMemcpyAsync) of `nbytes`, read and written once per copy: the bandwidth a
+    copy reaches on this GPU, next to the producers' algorithmic GB/s."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev).fill_(1)
+    dst = torch.empty_like(src)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dst.copy_(src)
+    _, per = time_launches(lambda: dst.copy_(src), reps, stream)
+    ms = sorted(per)[len(per) // 2]
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"gbs": round(2 * nbytes / (ms * 1e-3) / 1e9, 1), "bytes_copied": nbytes, "median_ms": round(ms, 4),
+            "copies": reps}
+
 
 def time_launches(fn, steps: int, stream, flush=None):
     """Run fn() `steps` times on `stream`, each bracketed by its own CUDA events.
@@ -342,6 +365,16 @@ def run_ours(args, rank, world, dev):
     }
 
     if rank == 0 and world == 1 and not args.no_extras:
+        args.sm_mhz_seen = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+        result["roofline"]["memcpy_d2d"] = memcpy_d2d_ceiling(dev, stream)
+        ipe = recorded_value("adaln_block_kernel", os.path.join(ROOT, "profiles", "inst_per_element.txt"))
+        if ipe is not None:
+            props = torch.cuda.get_device_properties(dev)
+            ms_issue = ROWS * COLS * ipe / (props.multi_processor_count * 4 * 32 * args.sm_mhz_seen * 1e6) * 1e3
+            result["roofline"]["issue_ceiling"] = {
+                "thread_inst_per_elem": ipe, "ms_at_full_issue": round(ms_issue, 4),
+                "issue_efficiency": round(ms_issue / launch_ms, 3), "sm_mhz": args.sm_mhz_seen,
+                "source": "ncu smsp__sass_thread_inst_executed.sum per element, profiles/inst_per_element.txt"}
         result["producers"] = measure_producers(h3q, dev, stream, args)
         result["e2e"] = measure_e2e(h3q, dev, stream, w, gsf, args)
         if not args.no_cpu_baseline:
@@ -418,6 +451,18 @@ def measure_producers(h3q, dev, stream, args):
         h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)
     _, per = time_launches(lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream), n, stream)
     res["swiglu_65280x18944"] = entry(swiglu_bytes(*gate.shape), per, gate.shape[0])
+    ipe = recorded_value("swiglu_kernel", os.path.join(ROOT, "profiles", "inst_per_element.txt"))
+    if ipe is not None:
+        # the instruction-issue bound: every SM sub-partition issuing one warp
+        # instruction per cycle at the clock seen under load
+        props = torch.cuda.get_device_properties(dev)
+        lanes_per_s = props.multi_processor_count * 4 * 32 * args.sm_mhz_seen * 1e6
+        ms_issue = gate.numel() * ipe / lanes_per_s * 1e3
+        res["swiglu_65280x18944"]["issue_ceiling"] = {
+            "thread_inst_per_elem": ipe, "ms_at_full_issue": round(ms_issue, 4),
+            "gbs_at_full_issue": round(swiglu_bytes(*gate.shape) / (ms_issue * 1e-3) / 1e9, 1),
+            "sm_mhz": args.sm_mhz_seen,
+            "source": "ncu smsp__sass_thread_inst_executed.sum per element, profiles/inst_per_element.txt"}
     del c, s
 
     # SwiGLU of the value-first packed projection with its bias, 65,280 x 2 x 18,944
@@ -545,11 +590,23 @@ def cpu_baseline(seconds: float = 15.0, rows_per_chunk: int = 255):
         done_rows += rows_per_chunk
         chunk += 1
     nbytes = done_rows / ROWS * adaln_bytes(ROWS, COLS, FRAMES)
+    # the same oracle on one core, over a shorter sample
+    one_rows, one_spent, one_chunk = 0, 0.0, 0
+    while one_spent < max(1.0, seconds / 5):
+        x, gm, tb, fr, eps = _oracle_adaln_sample(rows_per_chunk, seed=500 + one_chunk)
+        t0 = time.perf_counter()
+        oracle.adaln_rows(x, gm, tb, fr, eps, 1.0, threads=1)
+        one_spent += time.perf_counter() - t0
+        one_rows += rows_per_chunk
+        one_chunk += 1
+    one_bytes = one_rows / ROWS * adaln_bytes(ROWS, COLS, FRAMES)
     return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{done_rows} rows x {COLS} of the AdaLN workload ({chunk} chunks of "
                       f"{rows_per_chunk} rows, {spent:.1f} s on {threads} threads); GB/s by the "
-                      "same algorithmic-byte count as the GPU line"}
+                      "same algorithmic-byte count as the GPU line",
+            "single_core": {"value": round(one_bytes / one_spent / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"{one_rows} rows x {COLS} ({one_spent:.1f} s on one thread)"}}
 
 
 def run_reference(args, rank, world):

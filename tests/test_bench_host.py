@@ -25,3 +25,17 @@ def test_algorithmic_bytes():
     assert bench.adaln_bytes(65280, 7168, 32) == 1_199_994_884
     assert bench.quantize_bytes(8192, 7168) == 150_470_660
     assert bench.swiglu_bytes(65280, 18944) == 5_642_280_964
+
+
+def test_recorded_instruction_counts_follow_the_source_hash(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash("swiglu_kernel")
+    record = tmp_path / "inst_per_element.txt"
+    record.write_text(f"# comment\nswiglu_kernel {h} 20.037\n")
+    assert bench.recorded_value("swiglu_kernel", str(record)) == 20.037
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "f" * 16)
+    assert bench.recorded_value("swiglu_kernel", str(record)) is None
+
+
+def test_qkv_bytes():
+    # q, k, v read and written, three biases, cos and sin once
+    assert bench.qkv_bytes(65280, 56, 128, 64) == 3 * 2 * 65280 * 7168 * 2 + 3 * 7168 * 2 + 2 * 65280 * 64 * 2
