@@ -86,3 +86,19 @@ def test_full_workload_sampled_rows(dev):
     idx = workloads.sample_rows(w["q"].shape[0], random=1024).to(dev)
     want = _oracle(w, idx)
     _check([g.index_select(0, idx) for g in got], want, "qkv 65280x56x128")
+
+
+def test_past_2_31_elements_the_pages_regression_shape(dev):
+    """8,500,000 tokens x 2 heads x 128 per tensor (2.176e9 elements, the shape of
+    the FastVideo commit log's int64 fix for the q/k norm + partial RoPE kernel):
+    the first and last 256 rows and 512 random rows of q, k and v equal the
+    oracle's (the last rows sit past element 2^31)."""
+    rows = 8_500_000
+    w = workloads.qkv_inputs(dev, rows=rows, heads=2, head_dim=128, rot=64, seed=31)
+    assert w["q"].shape[0] * w["q"].shape[1] > 2 ** 31
+    got = _run(w)
+    torch.cuda.synchronize()
+    idx = workloads.sample_rows(rows, random=512).to(dev)
+    _check([g.index_select(0, idx) for g in got], _oracle(w, idx), "qkv 8.5M x 2 x 128")
+    del w, got
+    torch.cuda.empty_cache()
