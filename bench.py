@@ -410,16 +410,65 @@ def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
     total_ms, _ = time_launches(step, steps, stream)
     total_ms = max_over_ranks(total_ms, world, dev)
     nbytes = adaln_bytes(ROWS, COLS, FRAMES)
-    return {
+    h2d = hx.numel() * 2 + hg.numel() * 2 + ht.numel() * 2
+    d2h = hc.numel() + hs.numel()
+    out = {
         "value": round(job_gbs(nbytes, steps, world, total_ms), 1),
         "unit": "GB/s",
-        "h2d_bytes_per_step": hx.numel() * 2 + hg.numel() * 2 + ht.numel() * 2,
-        "d2h_bytes_per_step": hc.numel() + hs.numel(),
+        "h2d_bytes_per_step": h2d,
+        "d2h_bytes_per_step": d2h,
         "steps": steps,
         "ms_per_step": round(total_ms / steps, 3),
         "pipeline": {"chunk_rows": pipe.chunk_rows, "depth": pipe.depth, "streams": 3},
         "check": e2e_matches(h3q, dev, w, gsf, hc, hs),
     }
+    if world == 1:
+        link = host_link(dev)
+        bound = link_bound_ms(h2d, d2h, link)
+        out["host_link"] = dict(link, bound_ms_per_step=round(bound, 3),
+                                frac_of_link_bound=round(bound / (total_ms / steps), 3))
+    return out
+
+
+def host_link(dev, nbytes: int = 512 << 20, reps: int = 8) -> dict:
+    """Pinned host <-> device copy bandwidth on this machine: each direction alone and
+    both at once on two streams (GB/s per direction)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return reps * nbytes / (time.perf_counter() - t0) / 1e9
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    res = {"h2d_gbs": round(timed(lambda: d_in.copy_(h_in, non_blocking=True)), 1),
+           "d2h_gbs": round(timed(lambda: h_out.copy_(d_out, non_blocking=True)), 1),
+           "both_gbs_each": round(timed(both), 1), "bytes_per_copy": nbytes}
+    del h_in, h_out, d_in, d_out
+    return res
+
+
+def link_bound_ms(h2d_bytes: int, d2h_bytes: int, link: dict) -> float:
+    """The shortest step the host link allows: the smaller direction's bytes moved
+    while the larger one runs beside it (both at the two-way rate), the rest of the
+    larger direction alone."""
+    big, small = (h2d_bytes, d2h_bytes) if h2d_bytes >= d2h_bytes else (d2h_bytes, h2d_bytes)
+    big_rate = link["h2d_gbs"] if h2d_bytes >= d2h_bytes else link["d2h_gbs"]
+    return (small / (link["both_gbs_each"] * 1e9) + (big - small) / (big_rate * 1e9)) * 1e3
 
 
 def e2e_matches(h3q, dev, w, gsf, hc, hs) -> bool:

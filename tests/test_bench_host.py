@@ -39,3 +39,11 @@ def test_recorded_instruction_counts_follow_the_source_hash(tmp_path, monkeypatc
 def test_qkv_bytes():
     # q, k, v read and written, three biases, cos and sin once
     assert bench.qkv_bytes(65280, 56, 128, 64) == 3 * 2 * 65280 * 7168 * 2 + 3 * 7168 * 2 + 2 * 65280 * 64 * 2
+
+
+def test_link_bound():
+    link = {"h2d_gbs": 200.0, "d2h_gbs": 100.0, "both_gbs_each": 50.0}
+    # 1 GB in, 0.5 GB out: 0.5 GB each way at 50 GB/s (10 ms), then 0.5 GB in at 200 GB/s (2.5 ms)
+    assert abs(bench.link_bound_ms(10 ** 9, 5 * 10 ** 8, link) - 12.5) < 1e-9
+    # the larger direction out: its own one-way rate for the rest
+    assert abs(bench.link_bound_ms(5 * 10 ** 8, 10 ** 9, link) - 15.0) < 1e-9
