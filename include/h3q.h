@@ -93,7 +93,7 @@ static inline int64_t h3q_scale_offset_of_row_tile(int64_t row0, int64_t cols)
 }
 
 /*
- * (c) Standalone NVFP4 quantize, e.g. of the attention output viewed as
+ * Standalone NVFP4 quantize, e.g. of the attention output viewed as
  * [tokens, heads*head_dim].  (TensorRT-LLM PR #21483 "Fuse the MiniMax-H3
  * NVFP4 activation quantize into the AdaLN, SwiGLU and attention-output
  * producers", commit "...quantize it with a bandwidth-bound kernel";
@@ -108,7 +108,7 @@ int h3q_quantize_nvfp4(const void *x, int64_t ld_x, int64_t rows, int64_t cols,
                        void *stream);
 
 /*
- * (a) RMSNorm with fp32 statistics, AdaLN modulation, NVFP4.  (TensorRT-LLM
+ * RMSNorm with fp32 statistics, AdaLN modulation, NVFP4.  (TensorRT-LLM
  * PR #21483, summary and commit "...SwiGLU producers": the AdaLN RMSNorm +
  * modulation kernel emits packed E2M1 codes and swizzled E4M3 scales
  * directly; FastVideo API page, introduction: fp32 statistics, sequential
@@ -147,7 +147,7 @@ int h3q_rmsnorm_adaln_nvfp4(const void *x, int64_t ld_x, const void *gamma,
                             float *row_rstd, void *stream);
 
 /*
- * (b) SwiGLU producer: y = bf16(fl(fl(g * sigma) * u)) with
+ * SwiGLU producer: y = bf16(fl(fl(g * sigma) * u)) with
  * sigma = fl(1 / fl(1 + exp_c(-g))), then NVFP4.  (FastVideo compare page,
  * minimax_h3_swiglu_quant.cuh, swiglu_bf16: value * silu(gate) rounded to
  * bf16; TensorRT-LLM PR #21483, SiLU-and-mul producer.)  exp_c is a fixed

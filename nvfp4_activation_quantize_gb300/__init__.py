@@ -171,7 +171,7 @@ def _stream(stream, device) -> int:
 
 
 def h3q_quantize_nvfp4(x, global_scale, codes=None, scales=None, stream=None):
-    """(c) Standalone NVFP4 quantize of bf16 x [rows, cols]; returns (codes, scales)."""
+    """Standalone NVFP4 quantize of bf16 x [rows, cols]; returns (codes, scales)."""
     import torch
 
     x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
@@ -188,7 +188,7 @@ def h3q_quantize_nvfp4(x, global_scale, codes=None, scales=None, stream=None):
 def h3q_rmsnorm_adaln_nvfp4(x, gamma, mod_table, global_scale, *, row_frame=None,
                             rows_per_frame=None, eps=1e-6, codes=None, scales=None, row_rstd=None,
                             stream=None):
-    """(a) RMSNorm (fp32 statistics) + AdaLN modulation + NVFP4 of bf16 x [rows, cols].
+    """RMSNorm (fp32 statistics) + AdaLN modulation + NVFP4 of bf16 x [rows, cols].
 
     ``mod_table`` is bf16 [frames, 2, cols] ([t, 0] shift, [t, 1] scale); the frame
     of a row is ``row_frame[row]`` (int32 CUDA tensor) or ``row // rows_per_frame``.
@@ -227,7 +227,7 @@ def h3q_rmsnorm_adaln_nvfp4(x, gamma, mod_table, global_scale, *, row_frame=None
 
 
 def h3q_swiglu_nvfp4(gate, up, global_scale, codes=None, scales=None, stream=None):
-    """(b) NVFP4 of bf16(silu(gate) * up) for bf16 gate, up [rows, cols]; returns (codes, scales)."""
+    """NVFP4 of bf16(silu(gate) * up) for bf16 gate, up [rows, cols]; returns (codes, scales)."""
     import torch
 
     gate, rows, cols, ldg = _rows_view("gate", gate, torch.bfloat16)

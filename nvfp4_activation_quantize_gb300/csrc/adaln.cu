@@ -1,4 +1,4 @@
-// adaln.cu -- (a) RMSNorm with fp32 statistics + AdaLN modulation + NVFP4.
+// adaln.cu -- RMSNorm with fp32 statistics + AdaLN modulation + NVFP4.
 //
 // (TensorRT-LLM PR #21483, summary and commit "...SwiGLU producers": the AdaLN
 // RMSNorm + modulation kernel writes packed E2M1 codes and swizzled E4M3 block

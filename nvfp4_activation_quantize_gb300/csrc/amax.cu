@@ -1,4 +1,4 @@
-// amax.cu -- dynamic and calibrated global scales (NEXT row f3).
+// amax.cu -- dynamic and calibrated global scales.
 //
 // (FastVideo API page, NVFP4DecoderLinear: a dynamic layer scales each call by
 // the abs-max of its input, and calibration folds each call's abs-max into a

@@ -1,5 +1,4 @@
-// qkv.cu -- QKV epilogue: bias + per-head RMSNorm + partial rotate-half RoPE
-// (NEXT row f4).
+// qkv.cu -- QKV epilogue: bias + per-head RMSNorm + partial rotate-half RoPE.
 //
 // (FastVideo API page, qkv_epilogue: projected q/k/v [M, H*HD] bf16 with the
 // bias not yet added -> roped q, k and biased v, each [M, H, HD]; cos/sin are

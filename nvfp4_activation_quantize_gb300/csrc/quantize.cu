@@ -1,4 +1,4 @@
-// quantize.cu -- (c) standalone NVFP4 quantize of a bf16 [rows, cols] tensor,
+// quantize.cu -- standalone NVFP4 quantize of a bf16 [rows, cols] tensor,
 // e.g. the attention output viewed as [tokens, heads*head_dim].
 //
 // (TensorRT-LLM PR #21483, commit "...quantize it with a bandwidth-bound

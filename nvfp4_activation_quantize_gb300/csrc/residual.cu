@@ -1,5 +1,4 @@
-// residual.cu -- residual fold + RMSNorm (fp32 statistics) + AdaLN + NVFP4
-// (NEXT row f1).
+// residual.cu -- residual fold + RMSNorm (fp32 statistics) + AdaLN + NVFP4.
 //
 // (TensorRT-LLM PR #21483, commit "...norm1 ... from a second table": a block
 // folds its MLP residual into the next block's norm1 kernel, reading the gate

@@ -1,4 +1,4 @@
-// swiglu.cu -- (b) SwiGLU producer: y = silu(gate) * up rounded to bf16, then NVFP4.
+// swiglu.cu -- SwiGLU producer: y = silu(gate) * up rounded to bf16, then NVFP4.
 //
 // (FastVideo compare "fasth3-spark-exact-perf", minimax_h3_swiglu_quant.cuh,
 // swiglu_bf16: value * silu(gate), one bf16 rounding; TensorRT-LLM PR #21483,

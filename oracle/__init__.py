@@ -320,7 +320,7 @@ def row_rstd_f32(row: np.ndarray, eps: float) -> float:
 
 def residual_adaln_rows(h, o_bits, bias_bits, gate_bits, gamma_bits, table_bits, frames, eps: float,
                         gsf: float | None, want_y: bool = False, threads: int = 1):
-    """Residual fold + RMSNorm + AdaLN -> NVFP4 (NEXT row f1).
+    """Residual fold + RMSNorm + AdaLN -> NVFP4.
 
     ``h`` fp32 [n, cols] (not modified; the folded residual is returned), ``o``
     bf16 bits [n, cols], ``bias`` bf16 bits [cols] or None, ``gate`` bf16 bits

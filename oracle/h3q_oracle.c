@@ -275,7 +275,7 @@ void orc_quantize_block(const float y[16], float gsf, uint8_t *sf_out, uint8_t p
  * magnitude (6): gsf = fl(448 * 6 / amax). */
 float orc_global_scale(float amax) { return 2688.0f / amax; }
 
-/* Dynamic and calibrated scales (f3).  [FV-API] NVFP4DecoderLinear: a dynamic
+/* Dynamic and calibrated scales.  [FV-API] NVFP4DecoderLinear: a dynamic
  * layer scales each call by the abs-max of its input; a calibrating layer folds
  * each call's abs-max into a persistent running maximum (input_amax).
  * [FlashRT] commit "...amax pipeline": the abs-max is taken on the device in a
@@ -357,7 +357,7 @@ static void quantize_row_values(const float *y, int64_t cols, float gsf, uint8_t
         orc_quantize_block(y + 16 * b, gsf, &sf_row[b], &codes_row[8 * b]);
 }
 
-/* (c) standalone quantize, e.g. of the attention output ([TRT] commit
+/* standalone quantize, e.g. of the attention output ([TRT] commit
  * "quantize the attention output with a bandwidth-bound kernel";
  * [FV-API] quantize). */
 void orc_quantize_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t ld, float gsf,
@@ -415,7 +415,7 @@ float orc_row_rstd(const uint16_t *xrow, int64_t cols, float eps)
 }
 
 /*
- * (a) RMSNorm with fp32 statistics, then AdaLN modulation, then NVFP4
+ * RMSNorm with fp32 statistics, then AdaLN modulation, then NVFP4
  * ([TRT] commit "...emit the packed E2M1 codes and swizzled E4M3 block
  * scales directly" for the AdaLN RMSNorm + modulation producer).
  * The modulation table is bf16 [frames, 2, cols]: [t][0] is the shift and
@@ -454,10 +454,10 @@ void orc_adaln_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t ld,
     }
 }
 
-/* (b) SwiGLU silu(gate) * up, then NVFP4 ([TRT] SiLU-and-mul producer;
+/* SwiGLU silu(gate) * up, then NVFP4 ([TRT] SiLU-and-mul producer;
  * [FV-CUH] swiglu_bf16).  y_out as above. */
 /*
- * SwiGLU of a value-first packed projection with its bias (NEXT row f2).
+ * SwiGLU of a value-first packed projection with its bias.
  * [FV-API] swiglu_quantize: o is [M, 2F], value first (columns 0..F-1), gate
  * second, the bias not yet added.  Reading: each half gets its bias in binary32
  * and is rounded to bf16, as the projection's own output would be,
@@ -488,7 +488,7 @@ void orc_swiglu_packed_rows(const uint16_t *o, int64_t ld_o, const uint16_t *bia
 }
 
 /* ------------------------------------------------------------------------ */
-/* QKV epilogue: bias + per-head RMSNorm + partial RoPE (NEXT row f4)         */
+/* QKV epilogue: bias + per-head RMSNorm + partial RoPE                     */
 /* ------------------------------------------------------------------------ */
 /*
  * [FV-API] qkv_epilogue: projected q/k/v [M, H*HD] bf16 with the bias not yet
@@ -561,7 +561,7 @@ void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias
 }
 
 /* ------------------------------------------------------------------------ */
-/* Residual fold + RMSNorm + AdaLN (NEXT row f1)                              */
+/* Residual fold + RMSNorm + AdaLN                                          */
 /* ------------------------------------------------------------------------ */
 /*
  * [TRT] commit "...norm1 ... from a second table": a block folds its MLP

@@ -1,4 +1,4 @@
-"""GPU parity of the dynamic and calibrated global scales (NEXT row f3), through
+"""GPU parity of the dynamic and calibrated global scales, through
 the C ABI: each producer's abs-max pass equals the oracle's max |y| over the
 same bf16 outputs, the device global scale equals the oracle's, the running
 maximum folds across calls, and the chained dynamic call (abs-max pass, scale,

@@ -1,5 +1,5 @@
 """GPU parity of the QKV epilogue (bias + per-head RMSNorm + partial rotate-half
-RoPE on q and k, bias on v; NEXT row f4) through the C ABI: every output bf16 of
+RoPE on q and k, bias on v) through the C ABI: every output bf16 of
 q, k and v equals the oracle's, over head dims 64/128/256, rotary widths 0 to
 HD, odd head counts (a half-filled warp), strided views of one packed
 projection, and sampled rows of the 65,280-token workload the benchmark times."""

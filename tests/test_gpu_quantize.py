@@ -1,4 +1,4 @@
-"""GPU parity of the standalone quantize (c) and the dequantize, through the C ABI."""
+"""GPU parity of the standalone quantize and the dequantize, through the C ABI."""
 import numpy as np
 import pytest
 import torch

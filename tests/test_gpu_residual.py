@@ -1,7 +1,7 @@
-"""GPU parity of the residual fold + RMSNorm + AdaLN -> NVFP4 producer (NEXT row
-f1), through the C ABI: the folded residual written back to h (every fp32 bit),
-the codes and swizzled scales (every byte, padding rows zero) and each row's
-rstd equal the oracle's."""
+"""GPU parity of the residual fold + RMSNorm + AdaLN -> NVFP4 producer, through
+the C ABI: the folded residual written back to h (every fp32 bit), the codes and
+swizzled scales (every byte, padding rows zero) and each row's rstd equal the
+oracle's."""
 import numpy as np
 import pytest
 import torch

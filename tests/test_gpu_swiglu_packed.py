@@ -1,5 +1,5 @@
-"""GPU parity of the SwiGLU of a value-first packed projection with its bias
-(NEXT row f2), through the C ABI: every code and scale byte equals the oracle's,
+"""GPU parity of the SwiGLU of a value-first packed projection with its bias,
+through the C ABI: every code and scale byte equals the oracle's,
 with and without a bias, through the SiLU table and the direct path, for strided
 rows and the 65,280 x 18,944 workload."""
 import numpy as np

@@ -1,4 +1,4 @@
-"""The oracle's QKV epilogue (NEXT row f4) against what fixes it independently:
+"""The oracle's QKV epilogue against what fixes it independently:
 the bias add in numpy binary32 with torch's bf16 rounding; the per-head rstd
 equal to the AdaLN oracle's row rstd on the same 128 values (for a row of HD
 columns the two canonical orders coincide) and within 1e-6 of binary64; the

@@ -1,4 +1,4 @@
-"""The oracle's residual fold + RMSNorm + AdaLN (NEXT row f1) against what fixes it
+"""The oracle's residual fold + RMSNorm + AdaLN against what fixes it
 independently: the fold in numpy binary32 arithmetic with torch's bf16 rounding,
 exact hand values, the fp32-row rstd equal to the bf16-row rstd wherever the
 values are bf16, the whole norm part equal to the bf16 AdaLN oracle when the

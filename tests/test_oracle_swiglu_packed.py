@@ -1,4 +1,4 @@
-"""The oracle's SwiGLU of a value-first packed projection with bias (NEXT row f2)
+"""The oracle's SwiGLU of a value-first packed projection with bias
 against what fixes it independently: without a bias it is the separate-tensor
 SwiGLU oracle on the two halves (value = up, second half = gate); the bias add
 is binary32 addition rounded to bf16 by torch; hand values."""
