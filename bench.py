@@ -30,6 +30,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -103,12 +104,23 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without its comments and whitespace (string literals in
+    these sources hold no comment markers), so comment edits keep a record."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return "".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (comments and whitespace stripped) of the sources a
+    kernel is compiled from: records taken from a kernel stay valid until its
+    code changes."""
     csrc = os.path.join(ROOT, "nvfp4_activation_quantize_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

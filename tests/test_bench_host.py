@@ -47,3 +47,9 @@ def test_link_bound():
     assert abs(bench.link_bound_ms(10 ** 9, 5 * 10 ** 8, link) - 12.5) < 1e-9
     # the larger direction out: its own one-way rate for the rest
     assert abs(bench.link_bound_ms(5 * 10 ** 8, 10 ** 9, link) - 15.0) < 1e-9
+
+
+def test_source_hash_ignores_comments_and_whitespace():
+    code = "int f(int a) {\n  return a + 1;  // one\n}\n"
+    assert bench._code_only(code) == bench._code_only("/* header */\nint f(int a) { return a + 1; }")
+    assert bench._code_only(code) != bench._code_only("int f(int a) { return a + 2; }")
