@@ -152,7 +152,7 @@ __device__ __forceinline__ void swiglu_block_table(const Block16& g, const Block
     table_offsets(g.w[i], lo, hi);
     const float2 sv = make_float2(*reinterpret_cast<const float*>(table + lo),
                                   *reinterpret_cast<const float*>(table + hi));
-    y.w[i] = float2_to_bf16x2(mul2(sv, bf16x2_to_float2(u.w[i])));
+    y.w[i] = float2_to_bf16x2(mul2(sv, bf16x2_to_float2_fma(u.w[i])));
   }
 }
 
