@@ -250,11 +250,18 @@ __device__ __forceinline__ uint32_t block_scale(float amax, float gsf) {
   return e4m3_encode(__fmul_rn(gsf, amax_over_six(amax)));
 }
 
-// Codes of eight bf16 values (four words) under the inverse scale inv.
+// Codes of eight bf16 values (four words) under the inverse scale inv.  FMA:
+// unpack the bf16 values on the FMA pipe (kernels whose integer pipe is the
+// busier one); the codes are the same either way.
+template <bool FMA = false>
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+  return FMA ? bf16x2_to_float2_fma(w) : bf16x2_to_float2(w);
+}
+template <bool FMA = false>
 __device__ __forceinline__ uint32_t codes8(const uint32_t* w, float inv) {
   const float2 inv2 = make_float2(inv, inv);
-  return e2m1x8(mul2(bf16x2_to_float2_fma(w[0]), inv2), mul2(bf16x2_to_float2_fma(w[1]), inv2),
-                mul2(bf16x2_to_float2_fma(w[2]), inv2), mul2(bf16x2_to_float2_fma(w[3]), inv2));
+  return e2m1x8(mul2(unpack_bf16x2<FMA>(w[0]), inv2), mul2(unpack_bf16x2<FMA>(w[1]), inv2),
+                mul2(unpack_bf16x2<FMA>(w[2]), inv2), mul2(unpack_bf16x2<FMA>(w[3]), inv2));
 }
 
 struct Quantized {
@@ -265,13 +272,14 @@ struct Quantized {
 
 // NVFP4 of one block of bf16 values y under the global scale gsf:
 //   sf = E4M3(fl(gsf * fl(amax / 6))), inv = inv_table[sf], code_i = E2M1(fl(y_i * inv)).
+template <bool FMA = false>
 __device__ __forceinline__ Quantized quantize_block(const Block16& y, float gsf,
                                                     const float* inv_table) {
   Quantized q;
   q.sf = block_scale(block_amax(y), gsf);
   const float inv = inv_table[q.sf];
-  q.codes_lo = codes8(y.w, inv);
-  q.codes_hi = codes8(y.w + 4, inv);
+  q.codes_lo = codes8<FMA>(y.w, inv);
+  q.codes_hi = codes8<FMA>(y.w + 4, inv);
   return q;
 }
 

@@ -268,7 +268,7 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
         if (in_row && in_cols) run_max = fmaxf(run_max, block_amax(y));
         continue;
       }
-      Quantized q = quantize_block(y, gsf, inv_table);
+      Quantized q = quantize_block<true>(y, gsf, inv_table);
       if (!in_row) q.sf = 0;
       if (in_row && in_cols)
         store_codes(codes + row[u] * (cols >> 1) + g * 8, q.codes_lo, q.codes_hi);
