@@ -15,7 +15,10 @@
  * every s >= 0 whose low eight bits are zero plus every s within 256 ulps of one
  * of its decision points (the 127 values and the midpoints between neighbours,
  * where both formulations can change their result; between two decision points
- * both are constant).  Prints the mismatch counts and exits non-zero if any. */
+ * both are constant).  Also exp_c, the SiLU exponential: within 2 ulp of
+ * binary64 exp for every binary32 z in [-104, 88.7] (the ulp of the exact
+ * result's binary32 magnitude, the subnormal spacing below 2^-126), +inf above
+ * 89 and +0 below -104.  Prints the mismatch counts and exits non-zero if any. */
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -27,6 +30,15 @@
 uint16_t orc_bf16_bits(float v);
 uint8_t orc_e4m3_encode(float s);
 uint8_t orc_e2m1_encode(float v);
+float orc_exp(float z);
+
+/* spacing of binary32 values at the magnitude of x (x finite) */
+static double ulp_at(double x)
+{
+    float r = (float)fabs(x);
+    if (r < 0x1p-126f) return 0x1p-149;
+    return ldexp(1.0, ilogbf(r) - 23);
+}
 
 static float f_of(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
 
@@ -80,7 +92,7 @@ static uint8_t e4m3_ref(float s)
 
 static int full_e4m3;
 
-struct job { uint64_t first, last; unsigned long long bad[3]; };
+struct job { uint64_t first, last; unsigned long long bad[4]; double worst_exp_ulp; };
 
 static void *work(void *p)
 {
@@ -92,6 +104,14 @@ static void *work(void *p)
         if (orc_bf16_bits(v) != bf16_ref(v)) ++j->bad[0];
         if (orc_e2m1_encode(v) != e2m1_ref(v)) ++j->bad[1];
         if (!signbit(v) && (full_e4m3 || (u & 0xffu) == 0) && orc_e4m3_encode(v) != e4m3_ref(v)) ++j->bad[2];
+        if (v >= -104.0f && v <= 88.7f) {
+            double want = exp((double)v);
+            double err = fabs((double)orc_exp(v) - want) / ulp_at(want);
+            if (err > j->worst_exp_ulp) j->worst_exp_ulp = err;
+            if (err > 2.0) ++j->bad[3];
+        } else if ((v > 89.0f && !isinf(orc_exp(v))) || (v < -104.0f && orc_exp(v) != 0.0f)) {
+            ++j->bad[3];
+        }
     }
     return NULL;
 }
@@ -136,14 +156,18 @@ int main(int argc, char **argv)
         jobs[t].first = total * (uint64_t)t / (uint64_t)n;
         jobs[t].last = total * (uint64_t)(t + 1) / (uint64_t)n;
         memset(jobs[t].bad, 0, sizeof jobs[t].bad);
+        jobs[t].worst_exp_ulp = 0.0;
         pthread_create(&th[t], NULL, work, &jobs[t]);
     }
-    unsigned long long bad[3] = {0, 0, full_e4m3 ? 0 : e4m3_near_decisions()};
+    unsigned long long bad[4] = {0, 0, full_e4m3 ? 0 : e4m3_near_decisions(), 0};
+    double worst = 0.0;
     for (long t = 0; t < n; ++t) {
         pthread_join(th[t], NULL);
-        for (int k = 0; k < 3; ++k) bad[k] += jobs[t].bad[k];
+        for (int k = 0; k < 4; ++k) bad[k] += jobs[t].bad[k];
+        if (jobs[t].worst_exp_ulp > worst) worst = jobs[t].worst_exp_ulp;
     }
     printf("threads %ld bf16 mismatches %llu e2m1 mismatches %llu e4m3 (%s) mismatches %llu\n", n, bad[0],
            bad[1], full_e4m3 ? "every s >= 0" : "sampled and near every decision point", bad[2]);
-    return (bad[0] || bad[1] || bad[2]) ? 1 : 0;
+    printf("exp_c outside 2 ulp %llu worst %.4f ulp\n", bad[3], worst);
+    return (bad[0] || bad[1] || bad[2] || bad[3]) ? 1 : 0;
 }
