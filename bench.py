@@ -291,6 +291,13 @@ def calibrate_swiglu_gsf(gate, up) -> float:
 # our arm                                                                       #
 # --------------------------------------------------------------------------- #
 
+def workload_config() -> dict:
+    """The headline workload, named the same way by both arms."""
+    return {"workload": f"rmsnorm_adaln_nvfp4 {ROWS}x{COLS} bf16, {FRAMES} frames x {RPF} tokens, "
+                        "per-channel LogNormal(0,0.5) scales",
+            "rows": ROWS, "cols": COLS, "frames": FRAMES, "rows_per_frame": RPF}
+
+
 def run_ours(args, rank, world, dev):
     import nvfp4_activation_quantize_gb300 as h3q
 
@@ -350,9 +357,7 @@ def run_ours(args, rank, world, dev):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": f"rmsnorm_adaln_nvfp4 {ROWS}x{COLS} bf16, {FRAMES} frames x {RPF} tokens, "
-                        "per-channel LogNormal(0,0.5) scales",
-            "rows": ROWS, "cols": COLS, "frames": FRAMES, "rows_per_frame": RPF,
+            **workload_config(),
             "l2": f"inputs larger than L2 ({2 * ROWS * COLS / 1e6:.0f} MB bf16 read per step); no flush",
             "algorithmic_bytes_per_step": nbytes,
             "rows_per_s": round(world * ROWS * args.steps / (total_ms * 1e-3)),
@@ -689,16 +694,15 @@ def run_reference(args, rank, world):
             spent += time.perf_counter() - t0
     nbytes = rows_per_step / ROWS * adaln_bytes(ROWS, COLS, FRAMES) * args.steps
     value = round(nbytes / spent / 1e9, 4)
-    sample = (f"{rows_per_step} rows x {COLS} of the AdaLN workload per step, {threads} threads; "
-              "GB/s by the same algorithmic-byte count as the GPU line")
+    sample = (f"each step {rows_per_step} rows x {COLS} of the AdaLN workload (a bounded sample of its "
+              f"{ROWS} rows), {threads} threads; GB/s by the same algorithmic-byte count as the GPU line")
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"rmsnorm_adaln_nvfp4 {ROWS}x{COLS} bf16 (bounded row sample)",
-                   "rows_per_step": rows_per_step, "cols": COLS},
+        "config": {**workload_config(), "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
