@@ -624,6 +624,11 @@ def measure_producers(h3q, dev, stream, args):
     res["quantize_8192x7168_l2_flushed"] = entry(quantize_bytes(*x.shape), per, 8192)
     del x, c, s, scrub
     torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        for key, kind in (("swiglu_65280x18944", "swiglu"), ("swiglu_packed_bias_65280x18944", "swiglu_packed"),
+                          ("attn_out_quantize_65280x7168", "quantize"), ("residual_adaln_65280x7168", "residual"),
+                          ("qkv_epilogue_65280x56x128_rot64", "qkv")):
+            res[key]["cpu_oracle"] = producer_oracle(kind)
     return res
 
 
@@ -673,6 +678,60 @@ def cpu_baseline(seconds: float = 15.0, rows_per_chunk: int = 255):
                       "same algorithmic-byte count as the GPU line",
             "single_core": {"value": round(one_bytes / one_spent / 1e9, 4), "unit": "GB/s", "cores": 1,
                             "sample": f"{one_rows} rows x {COLS} ({one_spent:.1f} s on one thread)"}}
+
+
+def producer_oracle(kind: str, seconds: float = 2.0, rows: int = 64) -> dict:
+    """One producer's oracle as it stands on the host cores, over chunks of `rows`
+    rows of its workload until about `seconds` of work has run; GB/s by the same
+    algorithmic bytes per row as the GPU entry."""
+    import numpy as np
+    import oracle
+
+    threads = os.cpu_count() or 1
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    F = workloads.FFN
+    done, spent, chunk = 0, 0.0, 0
+    while spent < seconds:
+        seed = 300 + chunk
+        if kind == "swiglu":
+            gate, up = workloads.swiglu_inputs("cpu", rows=rows, seed=seed)
+            args_, fn = (bits(gate), bits(up), 1.0), oracle.swiglu_rows
+            per_row = swiglu_bytes(ROWS, F) / ROWS
+        elif kind == "swiglu_packed":
+            o, b = workloads.swiglu_packed_inputs("cpu", rows=rows, seed=seed)
+            args_, fn = (bits(o), bits(b), 1.0), oracle.swiglu_packed_rows
+            per_row = (swiglu_bytes(ROWS, F) + 4 * F) / ROWS
+        elif kind == "quantize":
+            x = workloads.attention_output("cpu", tokens=rows, seed=seed)
+            args_, fn = (bits(x), 1.0), oracle.quantize_rows
+            per_row = quantize_bytes(ROWS, COLS) / ROWS
+        elif kind == "residual":
+            w = workloads.residual_inputs("cpu", rows=rows, frames=1, seed=seed)
+            fr = np.zeros(rows, np.int64)
+            args_ = (w["h"].numpy(), bits(w["o"]), bits(w["bias"]), bits(w["gate"]), bits(w["gamma"]),
+                     bits(w["table"]), fr, w["eps"], 1.0)
+            fn = oracle.residual_adaln_rows
+            per_row = residual_bytes(ROWS, COLS, FRAMES) / ROWS
+        elif kind == "qkv":
+            w = workloads.qkv_inputs("cpu", rows=rows, seed=seed)
+            per_row = qkv_bytes(ROWS, w["heads"], w["head_dim"], w["rot"]) / ROWS
+            t0 = time.perf_counter()
+            for i, name in enumerate("qkv"):
+                oracle.qkv_epilogue_rows(bits(w[name]), bits(w["biases"][i]), w["heads"], bits(w["cos"]),
+                                         bits(w["sin"]), w["eps"], is_v=(name == "v"), threads=threads)
+            spent += time.perf_counter() - t0
+            done += rows
+            chunk += 1
+            continue
+        else:
+            raise ValueError(kind)
+        t0 = time.perf_counter()
+        fn(*args_, threads=threads)
+        spent += time.perf_counter() - t0
+        done += rows
+        chunk += 1
+    return {"gbs": round(done * per_row / spent / 1e9, 4), "cores": threads, "kind": "oracle",
+            "sample": f"{done} rows in {chunk} chunks of {rows}, {spent:.1f} s on {threads} threads"}
 
 
 def run_reference(args, rank, world):

@@ -53,3 +53,9 @@ def test_source_hash_ignores_comments_and_whitespace():
     code = "int f(int a) {\n  return a + 1;  // one\n}\n"
     assert bench._code_only(code) == bench._code_only("/* header */\nint f(int a) { return a + 1; }")
     assert bench._code_only(code) != bench._code_only("int f(int a) { return a + 2; }")
+
+
+def test_producer_oracle_timings_run_on_the_host():
+    for kind in ("swiglu", "swiglu_packed", "quantize", "residual", "qkv"):
+        r = bench.producer_oracle(kind, seconds=0.01, rows=8)
+        assert r["gbs"] > 0 and r["kind"] == "oracle" and r["cores"] >= 1
