@@ -1,9 +1,13 @@
 /*
  * h3q.h -- C ABI of the fused NVFP4 activation producers (GB300, sm_103a).
  *
- * Three producers turn bf16 activations into NVFP4 GEMM inputs with the
- * quantize fused into the kernel that produces them, plus a dequantize used
- * for checking.  Every producer writes:
+ * Producers that turn bf16 activations into NVFP4 GEMM inputs with the
+ * quantize fused into the kernel that produces them: RMSNorm + AdaLN, SwiGLU
+ * and the standalone (attention-output) quantize; the residual fold before the
+ * norm and the SwiGLU of a packed projection with its bias; abs-max passes for
+ * dynamic and calibrated global scales.  Beside them, the QKV epilogue (bias,
+ * per-head RMSNorm and rotate-half RoPE, bf16 outputs) and a dequantize used
+ * for checking.  Every NVFP4 producer writes:
  *
  *   codes   uint8 [rows, cols/2]: E2M1 codes, two per byte, the even column in
  *           the low nibble (FastVideo compare "fasth3-spark-exact-perf",
@@ -32,7 +36,8 @@
  *           `stream` has finished.
  * Stream    `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *           default stream).  Every call is asynchronous: it validates its
- *           arguments on the host, launches one kernel on `stream` and returns.
+ *           arguments on the host, launches its kernel on `stream` (the
+ *           dynamic-scale quantize launches three, in order) and returns.
  *           No call synchronises.  The device is the calling thread's current
  *           CUDA device.
  * Global    `global_scale` points to one fp32 on the device: the static
@@ -45,8 +50,9 @@
  *           multiple of 16.  Indexing is 64-bit throughout: inputs larger
  *           than 2^31 elements are supported (FastVideo commit log, branch
  *           vae-parallel-decode, the int64 program-id fix).
- * Alignment bf16 inputs and fp32 outputs: 32-byte aligned.  codes, scales:
- *           16-byte aligned.  row_frame, global_scale, row_rstd: 4-byte.
+ * Alignment bf16 inputs and fp32 outputs: 32-byte aligned.  codes, scales and
+ *           the QKV epilogue's bf16 outputs: 16-byte aligned.  row_frame,
+ *           global_scale, amax, row_rstd: 4-byte.
  * Aliasing  Outputs must not overlap inputs or each other.
  * Errors    H3Q_OK (0) on success.  H3Q_ERR_INVALID_ARGUMENT (1): an argument
  *           broke a rule above; nothing was launched and no output was
@@ -55,7 +61,10 @@
  *           h3q_last_error() returns a message for the calling thread's most
  *           recent failure.  No call aborts, traps or prints.
  * Threads   The calls keep no state between calls except a per-device cache
- *           of launch sizes; they are safe to call from several threads.
+ *           of launch sizes; they are safe to call from several threads.  The
+ *           one exception is h3q_quantize_nvfp4_dynamic, whose abs-max partials
+ *           live in a device array inside the library: calls of it that
+ *           overlap on one device race (see there).
  */
 #ifndef H3Q_H
 #define H3Q_H
