@@ -578,6 +578,12 @@ def measure_producers(h3q, dev, stream, args):
     res["adaln_dynamic_scale_65280x7168"] = entry(adaln_bytes(ROWS, COLS, FRAMES), per, ROWS)
     res["adaln_dynamic_scale_65280x7168"]["note"] = ("abs-max pass + device scale + producer; x is read "
                                                      "twice, GB/s by the single-pass bytes")
+    # the least a per-call abs-max scale can move: x read by both passes (the whole
+    # tensor's maximum is needed before any row is quantized), the outputs once
+    two_pass = adaln_bytes(ROWS, COLS, FRAMES) + 2 * ROWS * COLS + 2 * COLS + FRAMES * 2 * COLS * 2
+    dyn = res["adaln_dynamic_scale_65280x7168"]
+    dyn["two_pass_algorithmic_bytes"] = two_pass
+    dyn["frac_of_peak_two_pass"] = round(two_pass / (dyn["median_launch_ms"] * 1e-3) / 1e9 / peak, 4)
     del w, c, s
 
     # residual fold + RMSNorm + AdaLN: h (fp32) is read and written back each launch
