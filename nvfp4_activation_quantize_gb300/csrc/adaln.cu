@@ -70,22 +70,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint4 load16_reused(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint4 load16_stream(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ int64_t clamp_frame(const AdalnArgs& a, int64_t t) {
   return t < 0 ? 0 : (t >= a.num_frames ? a.num_frames - 1 : t);  // memory safety only
 }
@@ -194,12 +178,6 @@ __device__ __forceinline__ void row_sums(const float2 (&acc)[R][4], float (*tota
 __device__ __forceinline__ float rstd_of(float ss, float cols, float eps) {
   const float mean = __fdiv_rn(ss, cols);
   return __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
-}
-
-// Byte offset of row r's part of a scale word: everything of the swizzled index
-// but the scale-column quad (which adds quad * 512).
-__device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
-  return (r >> 7) * quads * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
 // Modulate one chunk of R rows (x words v[k], statistics rstd[k]) with the

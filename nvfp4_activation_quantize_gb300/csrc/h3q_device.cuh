@@ -46,6 +46,29 @@ __device__ __forceinline__ void load_reused(const void* p, Block16& b) {
                : "l"(p));
 }
 
+// 16-byte global accesses: streamed data read once (no L1 allocation), small
+// read-only tables re-read across rows (L1-allocating), and a 16-byte store.
+__device__ __forceinline__ uint4 load16_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 load16_reused(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void store16(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void store_codes(uint8_t* p, uint32_t lo, uint32_t hi) {
   asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
 }
@@ -319,6 +342,12 @@ __device__ __forceinline__ int64_t scale_word_offset(int64_t row, int64_t quad,
                                                      int64_t quads_per_row) {
   const int64_t atom = (row >> 7) * quads_per_row + quad;
   return atom * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+}
+
+// Byte offset of row r's part of a scale word: everything of scale_word_offset
+// but the scale-column quad (which adds quad * 512).
+__device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
+  return (r >> 7) * quads * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
 // Lanes 4a..4a+3 of a warp hold the scale bytes of four consecutive scale

@@ -43,28 +43,6 @@ struct QkvArgs {
   float eps;
 };
 
-__device__ __forceinline__ uint4 ld16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint4 ld16_reused(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void st16(void* p, uint4 v) {
-  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
 // bf16 pair w with its sign bits flipped: the exact negation of both values.
 __device__ __forceinline__ uint32_t neg_bf16x2(uint32_t w) { return w ^ 0x80008000u; }
 
@@ -101,7 +79,7 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
       xw[j] = make_uint4(0u, 0u, 0u, 0u);
       if (head < heads) {
         const int col = (g0 + j) * (kHeadsPerWarp * kHd) + col0;
-        xw[j] = ld16(xrow + col);
+        xw[j] = load16_stream(xrow + col);
       }
     }
 #pragma unroll
@@ -110,11 +88,11 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
       const int head = (g0 + j) * kHeadsPerWarp + lane / LPH;
       const int col = (g0 + j) * (kHeadsPerWarp * kHd) + col0;
       uint4 bw = make_uint4(0u, 0u, 0u, 0u);
-      if (head < heads) bw = ld16_reused(bias + col);
+      if (head < heads) bw = load16_reused(bias + col);
       uint32_t xb[4];
       biased(xw[j], bw, xb);
       if constexpr (!NORM) {
-        if (head < heads) st16(orow + col, make_uint4(xb[0], xb[1], xb[2], xb[3]));
+        if (head < heads) store16(orow + col, make_uint4(xb[0], xb[1], xb[2], xb[3]));
       } else {
         // the head's sum of squares: eight fmaf partials, the chunk total, a
         // butterfly over the head's lanes
@@ -151,7 +129,7 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
           }
           res = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        if (head < heads) st16(orow + col, res);
+        if (head < heads) store16(orow + col, res);
       }
     }
   }
@@ -185,8 +163,8 @@ __global__ void __launch_bounds__(kThreads) qkv_epilogue_kernel(const QkvArgs a)
     } else {
       uint4 cw = make_uint4(0u, 0u, 0u, 0u), sw = make_uint4(0u, 0u, 0u, 0u);
       if (c < rot_chunks) {
-        cw = ld16_reused(a.cos + row * a.rot + c * 8);
-        sw = ld16_reused(a.sin + row * a.rot + c * 8);
+        cw = load16_reused(a.cos + row * a.rot + c * 8);
+        sw = load16_reused(a.sin + row * a.rot + c * 8);
       }
       qkv_unit<LPH, U, true>(xrow, a.bias[tensor], orow, heads, lane, c, src, half, rot_chunks, cw, sw,
                              a.eps);

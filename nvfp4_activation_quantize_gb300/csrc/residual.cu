@@ -59,14 +59,6 @@ __device__ __forceinline__ int64_t frame_of(const ResidualArgs& a, int64_t row) 
   return t < 0 ? 0 : (t >= a.num_frames ? a.num_frames - 1 : t);  // memory safety only
 }
 
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Eight fp32 of h: a 256-bit load (h is read once, written back by this kernel).
 __device__ __forceinline__ void ld_h8(const float* p, float (&v)[8]) {
   asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -79,10 +71,6 @@ __device__ __forceinline__ void st_h8(float* p, const float (&v)[8]) {
   asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
                "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
                : "memory");
-}
-
-__device__ __forceinline__ int64_t scale_row_offset(int64_t r, int64_t quads) {
-  return (r >> 7) * quads * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
 // Shared-memory tables, one 16-byte entry per 8-column chunk c (lane-consecutive,
@@ -111,10 +99,10 @@ __device__ __forceinline__ Tables carve(uint4* smem, int chunk_slots) {
 __device__ __forceinline__ void load_frame_tables(const ResidualArgs& a, const Tables& tb,
                                                   int64_t f, int64_t chunks) {
   for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-    tb.gate[c] = ld_stream16(a.gate + f * a.cols + c * 8);
+    tb.gate[c] = load16_stream(a.gate + f * a.cols + c * 8);
     const uint16_t* shift = a.table + f * 2 * a.cols + c * 8;
-    tb.shift[c] = ld_stream16(shift);
-    const uint4 sc = ld_stream16(shift + a.cols);
+    tb.shift[c] = load16_stream(shift);
+    const uint4 sc = load16_stream(shift + a.cols);
     const float2 s0 = add2(make_float2(1.0f, 1.0f), bf16x2_to_float2(sc.x));
     const float2 s1 = add2(make_float2(1.0f, 1.0f), bf16x2_to_float2(sc.y));
     const float2 s2 = add2(make_float2(1.0f, 1.0f), bf16x2_to_float2(sc.z));
@@ -196,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 2) residual_adaln_kernel(const Resid
   const float cols_f = static_cast<float>(a.cols);  // exact: cols <= 2^24
   const bool has_bias = a.bias != nullptr;
   for (int64_t c = t; c < chunks; c += kThreads) {  // the launch-wide tables
-    tb.gamma[c] = ld_stream16(a.gamma + c * 8);
-    if (has_bias) tb.bias[c] = ld_stream16(a.bias + c * 8);
+    tb.gamma[c] = load16_stream(a.gamma + c * 8);
+    if (has_bias) tb.bias[c] = load16_stream(a.bias + c * 8);
   }
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
   const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
@@ -211,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2) residual_adaln_kernel(const Resid
     for (int j = 0; j < C1; ++j) {
       if (FULL || t + j * kThreads < chunks) {
         ld_h8(hr + j * (kThreads * 8), h[j]);
-        o[j] = ld_stream16(orow + j * (kThreads * 8));
+        o[j] = load16_stream(orow + j * (kThreads * 8));
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[j][e] = 0.0f;
