@@ -69,7 +69,8 @@ _SIGNATURES = {
     "orc_global_scale": ([_F], _F),
     "orc_amax_bf16": ([_P, _I64], _F),
     "orc_row_rstd_f32": ([_P, _I64, _F], _F),
-    "orc_qkv_epilogue_rows": ([_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _I64, _F, _P], None),
+    "orc_qkv_epilogue_rows": ([_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _I64, ctypes.c_int, _F,
+                               _P], None),
     "orc_swiglu_packed_rows": ([_P, _I64, _P, _I64, _I64, _F, _P, _P, _P, _P], None),
     "orc_residual_adaln_rows": ([_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P, _P], None),
     "orc_global_scale_from_amax": ([_F], _F),
@@ -411,10 +412,11 @@ def swiglu_packed_rows(o_bits, bias_bits, gsf: float | None, want_y: bool = Fals
 
 
 def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: float, is_v: bool,
-                      threads: int = 1) -> np.ndarray:
+                      threads: int = 1, interleaved: bool = False) -> np.ndarray:
     """QKV epilogue of one projected tensor x [n, heads * HD] (bf16 bits) with its bias
     [heads * HD]: v gets the bias only; q and k the bias, the per-head RMSNorm and the
-    rotate-half RoPE on the first ROT values of each head (cos, sin bf16 [n, ROT]).
+    RoPE on the first ROT values of each head (cos, sin bf16 [n, ROT]): rotate-half
+    pairs (i, i + ROT/2), or with `interleaved` the pairs (2j, 2j + 1).
     Returns bf16 bits [n, heads, HD]."""
     x = _u16(x_bits)
     n, d = x.shape
@@ -431,7 +433,8 @@ def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: fl
     def work(span):
         a, b = span
         lib().orc_qkv_epilogue_rows(_ptr(x[a:b]), d, _ptr(bias), b - a, heads, hd, int(is_v),
-                                    _ptr(cos[a:b]), _ptr(sin[a:b]), rot, float(eps), _ptr(out[a:b]))
+                                    _ptr(cos[a:b]), _ptr(sin[a:b]), rot, int(interleaved), float(eps),
+                                    _ptr(out[a:b]))
 
     _run(work, n, threads)
     return out

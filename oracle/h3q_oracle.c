@@ -505,6 +505,9 @@ void orc_swiglu_packed_rows(const uint16_t *o, int64_t ld_o, const uint16_t *bia
  *     r_i = -n_{i+ROT/2} (i < ROT/2), n_{i-ROT/2} (ROT/2 <= i < ROT)
  *     out_i = bf16(fl(bf16(fl(n_i * cos_i)) + bf16(fl(r_i * sin_i))))   i < ROT
  *     out_i = n_i                                                         i >= ROT
+ *   or, with `interleaved`, the pairs (2j, 2j+1) rotated together ([FlashRT]
+ *   commit "...fused RMSNorm+RoPE kernels": interleaved RoPE on the native
+ *   [B, S, H, D] layout): r_{2j} = -n_{2j+1}, r_{2j+1} = n_{2j}, same out_i.
  */
 static float head_rstd(const float *v, int64_t hd, float eps)
 {
@@ -528,7 +531,8 @@ static float head_rstd(const float *v, int64_t hd, float eps)
 
 void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias, int64_t nrows,
                            int64_t heads, int64_t hd, int is_v, const uint16_t *cos_t,
-                           const uint16_t *sin_t, int64_t rot, float eps, uint16_t *out)
+                           const uint16_t *sin_t, int64_t rot, int interleaved, float eps,
+                           uint16_t *out)
 {
     float xb[1024], n[1024];
     for (int64_t r = 0; r < nrows; ++r) {
@@ -551,7 +555,11 @@ void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias
                     oh[i] = orc_bf16_bits(n[i]);
                     continue;
                 }
-                float rr = i < rot / 2 ? -n[i + rot / 2] : n[i - rot / 2];
+                float rr;
+                if (interleaved)
+                    rr = (i & 1) ? n[i - 1] : -n[i + 1];
+                else
+                    rr = i < rot / 2 ? -n[i + rot / 2] : n[i - rot / 2];
                 float a = orc_bf16_round(n[i] * orc_bf16_value(cos_t[r * rot + i]));
                 float b = orc_bf16_round(rr * orc_bf16_value(sin_t[r * rot + i]));
                 oh[i] = orc_bf16_bits(a + b);

@@ -89,3 +89,40 @@ def test_no_tables_is_the_norm_without_a_rotation():
     x, b, _, _ = _inputs(n, heads, 64, 12)
     got = oracle.qkv_epilogue_rows(x, b, heads, None, None, 1e-6, is_v=False)
     assert np.array_equal(got, _normed(x, b, heads, n))
+
+
+@pytest.mark.parametrize("rot", [16, 64, 128])
+def test_interleaved_rope_op_by_op(rot):
+    """Pairs (2j, 2j+1) rotated together: r_2j = -n_2j+1, r_2j+1 = n_2j."""
+    n, heads = 5, 2
+    x, b, cos, sin = _inputs(n, heads, rot, rot + 1)
+    nrm = _val(_normed(x, b, heads, n))
+    out = _val(oracle.qkv_epilogue_rows(x, b, heads, cos, sin, 1e-6, is_v=False, interleaved=True))
+    c, s = _val(cos)[:, None, :], _val(sin)[:, None, :]
+    first = nrm[..., :rot]
+    rotated = np.empty_like(first)
+    rotated[..., 0::2] = -first[..., 1::2]
+    rotated[..., 1::2] = first[..., 0::2]
+    want = _r(_r(first * c) + _r(rotated * s))
+    assert np.array_equal(out[..., :rot].view(np.uint32), want.view(np.uint32))
+    assert np.array_equal(out[..., rot:].view(np.uint32), nrm[..., rot:].view(np.uint32))
+
+
+def test_interleaved_is_rotate_half_in_permuted_coordinates():
+    """Interleaved RoPE on a head equals rotate-half RoPE on the head with its first
+    ROT values permuted (element 2j -> j, 2j+1 -> j + ROT/2) and cos/sin permuted the
+    same way, permuted back: the norm is order-independent only in exact arithmetic,
+    so the heads here are built so every partial sum is exact (values in {0, +-1, +-2})."""
+    n, heads, rot = 4, 3, 64
+    rng = np.random.default_rng(21)
+    x = _bf16(rng.choice([-2.0, -1.0, 0.0, 1.0, 2.0], size=(n, heads * HD)))
+    b = _bf16(np.zeros(heads * HD))
+    _, _, cos, sin = _inputs(n, heads, rot, 22)
+    perm = np.concatenate([np.arange(0, rot, 2), np.arange(1, rot, 2), np.arange(rot, HD)])
+    xp = x.reshape(n, heads, HD)[..., perm].reshape(n, heads * HD)
+    cp, sp = cos[:, perm[:rot]], sin[:, perm[:rot]]
+    half = oracle.qkv_epilogue_rows(xp, b, heads, cp, sp, 1e-6, is_v=False)
+    inter = oracle.qkv_epilogue_rows(x, b, heads, cos, sin, 1e-6, is_v=False, interleaved=True)
+    back = np.empty_like(half)
+    back[..., perm] = half
+    assert np.array_equal(back, inter)
