@@ -79,7 +79,7 @@ extern "C" {
 #define H3Q_ERR_INVALID_ARGUMENT 1
 #define H3Q_ERR_CUDA 2
 
-#define H3Q_ABI_VERSION 1
+#define H3Q_ABI_VERSION 2
 
 /* Rows of the scale matrix: rows rounded up to a multiple of 128. */
 static inline int64_t h3q_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
@@ -306,14 +306,17 @@ int h3q_quantize_nvfp4_dynamic(const void *x, int64_t ld_x, int64_t rows, int64_
  *          a butterfly over the head's HD/8 chunk totals);
  *          rstd = fl(1 / fl(sqrt(fl(fl(ss / HD) + eps)))), n = bf16(fl(x' * rstd));
  *          out_i = bf16(fl(bf16(fl(n_i * cos_i)) + bf16(fl(r_i * sin_i)))) for
- *          i < ROT, r_i = -n_{i+ROT/2} (i < ROT/2) or n_{i-ROT/2}; out_i = n_i
- *          for i >= ROT.
+ *          i < ROT, r_i = -n_{i+ROT/2} (i < ROT/2) or n_{i-ROT/2} (rotate-half
+ *          pairs), or with `interleaved` r_{2j} = -n_{2j+1}, r_{2j+1} = n_{2j}
+ *          (FlashRT PR #142 page, the fused RMSNorm + RoPE kernel: interleaved
+ *          RoPE on the [B, S, H, D] layout); out_i = n_i for i >= ROT.
  *
  *   q, k, v        bf16 [rows, heads * head_dim], row strides ld_q, ld_k, ld_v
  *                  (>= heads * head_dim, multiples of 16), 32-byte aligned.
  *   bias_q/k/v     bf16 [heads * head_dim], 32-byte aligned, not NULL.
  *   cos, sin       bf16 [rows, rot] contiguous, 16-byte aligned; NULL when rot = 0.
  *   rot            ROT, a multiple of 16 with 0 <= rot <= head_dim.
+ *   interleaved    0: rotate-half pairs (i, i + ROT/2); 1: pairs (2j, 2j + 1).
  *   heads          H >= 1; head_dim HD in {64, 128, 256}; heads * head_dim <= 2^24.
  *   eps            finite, >= 0.
  *   q_out, k_out, v_out  bf16 [rows, heads, head_dim] contiguous, 16-byte
@@ -323,9 +326,9 @@ int h3q_quantize_nvfp4_dynamic(const void *x, int64_t ld_x, int64_t rows, int64_
  */
 int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, const void *v,
                      int64_t ld_v, const void *bias_q, const void *bias_k, const void *bias_v,
-                     const void *cos, const void *sin, int64_t rot, int64_t rows, int64_t heads,
-                     int64_t head_dim, float eps, void *q_out, void *k_out, void *v_out,
-                     void *stream);
+                     const void *cos, const void *sin, int64_t rot, int interleaved, int64_t rows,
+                     int64_t heads, int64_t head_dim, float eps, void *q_out, void *k_out,
+                     void *v_out, void *stream);
 
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char *h3q_last_error(void);

@@ -47,8 +47,8 @@ _SIGNATURES = {
     "h3q_swiglu_packed_nvfp4": [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P],
     "h3q_residual_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _I64,
                                          ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P],
-    "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
-                         ctypes.c_float, _P, _P, _P, _P],
+    "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _I64, _I64,
+                         _I64, ctypes.c_float, _P, _P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -454,11 +454,12 @@ def h3q_swiglu_packed_nvfp4(o, global_scale, bias=None, codes=None, scales=None,
     return codes, scales
 
 
-def h3q_qkv_epilogue(q, k, v, biases, cos, sin, heads, eps, outs=None, stream=None):
+def h3q_qkv_epilogue(q, k, v, biases, cos, sin, heads, eps, outs=None, interleaved=False, stream=None):
     """QKV epilogue of projected q, k, v [rows, heads * HD] bf16 (bias not yet added):
     returns (q_out, k_out, v_out), each bf16 [rows, heads, HD], with q and k biased,
-    RMS-normed per head and rotated (rotate-half RoPE on each head's first ROT
-    values, cos and sin bf16 [rows, ROT]; None for ROT = 0) and v biased."""
+    RMS-normed per head and rotated (RoPE on each head's first ROT values, cos and
+    sin bf16 [rows, ROT], None for ROT = 0: rotate-half pairs (i, i + ROT/2), or
+    pairs (2j, 2j + 1) with ``interleaved``) and v biased."""
     import torch
 
     q, rows, d, ld_q = _rows_view("q", q, torch.bfloat16)
@@ -484,7 +485,8 @@ def h3q_qkv_epilogue(q, k, v, biases, cos, sin, heads, eps, outs=None, stream=No
     with torch.cuda.device(dev):
         rc = library().h3q_qkv_epilogue(q.data_ptr(), ld_q, k.data_ptr(), ld_k, v.data_ptr(), ld_v,
                                         b[0].data_ptr(), b[1].data_ptr(), b[2].data_ptr(), cos_ptr,
-                                        sin_ptr, rot, rows, heads, hd, float(eps), outs[0].data_ptr(),
+                                        sin_ptr, rot, int(bool(interleaved)), rows, heads, hd, float(eps),
+                                        outs[0].data_ptr(),
                                         outs[1].data_ptr(), outs[2].data_ptr(), _stream(stream, dev))
     _check("h3q_qkv_epilogue", rc)
     return outs[0], outs[1], outs[2]

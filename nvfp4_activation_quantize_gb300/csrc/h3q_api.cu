@@ -448,9 +448,9 @@ int h3q_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t ro
 
 int h3q_qkv_epilogue(const void* q, int64_t ld_q, const void* k, int64_t ld_k, const void* v,
                      int64_t ld_v, const void* bias_q, const void* bias_k, const void* bias_v,
-                     const void* cos, const void* sin, int64_t rot, int64_t rows, int64_t heads,
-                     int64_t head_dim, float eps, void* q_out, void* k_out, void* v_out,
-                     void* stream) {
+                     const void* cos, const void* sin, int64_t rot, int interleaved, int64_t rows,
+                     int64_t heads, int64_t head_dim, float eps, void* q_out, void* k_out,
+                     void* v_out, void* stream) {
   static const char* fn = "h3q_qkv_epilogue";
   g_last_error.clear();
   if (rows < 0) return invalid(fn, "rows must be >= 0");
@@ -461,6 +461,7 @@ int h3q_qkv_epilogue(const void* q, int64_t ld_q, const void* k, int64_t ld_k, c
   if (heads > kMaxCols / head_dim) return invalid(fn, "heads * head_dim exceeds 2^24");
   if (rot < 0 || rot > head_dim || rot % 16 != 0)
     return invalid(fn, "rot must be a multiple of 16 in [0, head_dim]");
+  if (interleaved != 0 && interleaved != 1) return invalid(fn, "interleaved must be 0 or 1");
   if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
   if (rows == 0) return H3Q_OK;
   const int64_t d = heads * head_dim;
@@ -508,7 +509,7 @@ int h3q_qkv_epilogue(const void* q, int64_t ld_q, const void* k, int64_t ld_k, c
   }
   cudaError_t err = h3q::launch_qkv_epilogue(
       x16, lds, b16, o16, static_cast<const uint16_t*>(cos), static_cast<const uint16_t*>(sin), rot,
-      rows, heads, head_dim, eps, static_cast<cudaStream_t>(stream));
+      interleaved, rows, heads, head_dim, eps, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 

@@ -67,11 +67,13 @@ cudaError_t launch_swiglu_packed(const uint16_t* o, int64_t ld_o, const uint16_t
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                               int64_t cols, const float* gsf, float* out, cudaStream_t stream);
 
-// QKV epilogue over q, k, v (index 0, 1, 2): bias, per-head RMSNorm and
-// rotate-half RoPE on q and k, bias on v; head_dim in {64, 128, 256}.
+// QKV epilogue over q, k, v (index 0, 1, 2): bias, per-head RMSNorm and RoPE
+// (rotate-half pairs, or interleaved pairs when `interleaved`) on q and k, bias
+// on v; head_dim in {64, 128, 256}.
 cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
                                 const uint16_t* const bias[3], uint16_t* const out[3],
-                                const uint16_t* cos, const uint16_t* sin, int64_t rot, int64_t rows,
-                                int64_t heads, int64_t head_dim, float eps, cudaStream_t stream);
+                                const uint16_t* cos, const uint16_t* sin, int64_t rot, int interleaved,
+                                int64_t rows, int64_t heads, int64_t head_dim, float eps,
+                                cudaStream_t stream);
 
 }  // namespace h3q

@@ -38,6 +38,7 @@ struct QkvArgs {
   const uint16_t* cos;  // [rows, rot]
   const uint16_t* sin;
   int64_t rot;
+  int interleaved;  // RoPE pairs (2j, 2j+1) instead of (i, i + ROT/2)
   int64_t rows;
   int64_t heads;
   float eps;
@@ -45,6 +46,11 @@ struct QkvArgs {
 
 // bf16 pair w with its sign bits flipped: the exact negation of both values.
 __device__ __forceinline__ uint32_t neg_bf16x2(uint32_t w) { return w ^ 0x80008000u; }
+
+// The interleaved rotation partner of a bf16 pair (n_2j, n_2j+1): (-n_2j+1, n_2j).
+__device__ __forceinline__ uint32_t rot_pair_bf16x2(uint32_t w) {
+  return __byte_perm(w, 0, 0x1032) ^ 0x00008000u;
+}
 
 // x' = bf16(fl(x + b)) for the eight values of a chunk (one bf16x2 add per
 // pair: the same bits, see add_bf16x2).
@@ -57,11 +63,13 @@ __device__ __forceinline__ void biased(const uint4& xw, const uint4& bw, uint32_
 
 // One (row, tensor) unit: the row's heads of q, k or v, `kHeadsPerWarp` at a
 // time, U head groups per batch with all their x loads issued before any use.
+// ILV: interleaved RoPE pairs (2j, 2j+1), whose partner is the other half of the
+// same bf16 pair; otherwise rotate-half pairs (i, i + ROT/2), one shuffle away.
 // The bias is loaded where it is used: it is re-read by every row and stays in
 // L1, and keeping U bias chunks live would cost the registers (and so the
 // resident warps) that hold the loads of x in flight.
 // NORM: q or k (norm and rotation); otherwise v (the bias only).
-template <int LPH, int U, bool NORM>
+template <int LPH, int U, bool NORM, bool ILV>
 __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
                                          const uint16_t* __restrict__ bias, uint16_t* __restrict__ orow,
                                          int heads, int lane, int c, int src, int half, int rot_chunks,
@@ -111,10 +119,17 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
         uint32_t nw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) nw[i] = float2_to_bf16x2(mul2(bf16x2_to_float2(xb[i]), rstd2));
-        // rotate-half RoPE on the head's first ROT values
-        uint32_t pw[4];
+        // RoPE on the head's first ROT values: r, the rotation partner of each value
+        uint32_t rw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) pw[i] = __shfl_sync(0xffffffffu, nw[i], src);
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (ILV) {
+            rw[i] = rot_pair_bf16x2(nw[i]);
+          } else {
+            const uint32_t pw = __shfl_sync(0xffffffffu, nw[i], src);
+            rw[i] = c < half ? neg_bf16x2(pw) : pw;
+          }
+        }
         uint4 res = make_uint4(nw[0], nw[1], nw[2], nw[3]);
         if (c < rot_chunks) {
           const uint32_t cs[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -122,9 +137,8 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
           uint32_t o[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t r = c < half ? neg_bf16x2(pw[i]) : pw[i];
             const uint32_t p1 = float2_to_bf16x2(mul2(bf16x2_to_float2(nw[i]), bf16x2_to_float2(cs[i])));
-            const uint32_t p2 = float2_to_bf16x2(mul2(bf16x2_to_float2(r), bf16x2_to_float2(sn[i])));
+            const uint32_t p2 = float2_to_bf16x2(mul2(bf16x2_to_float2(rw[i]), bf16x2_to_float2(sn[i])));
             o[i] = add_bf16x2(p1, p2);  // bf16(fl(p1 + p2)) of two bf16 values
           }
           res = make_uint4(o[0], o[1], o[2], o[3]);
@@ -138,8 +152,8 @@ __device__ __forceinline__ void qkv_unit(const uint16_t* __restrict__ xrow,
 // HD = 8 * LPH: LPH lanes per head, 32 / LPH heads per warp.  Persistent warps
 // walk the (row, tensor) units with the row outermost, so the three units of a
 // row (which share its cos/sin) run on neighbouring warps.
-template <int LPH, int U>
-__global__ void __launch_bounds__(kThreads) qkv_epilogue_kernel(const QkvArgs a) {
+template <int LPH, int U, bool ILV>
+__global__ void __launch_bounds__(kThreads, 4) qkv_epilogue_kernel(const QkvArgs a) {
   const int lane = threadIdx.x & 31;
   const int c = lane % LPH;  // chunk of the head
   const int heads = static_cast<int>(a.heads);
@@ -159,15 +173,15 @@ __global__ void __launch_bounds__(kThreads) qkv_epilogue_kernel(const QkvArgs a)
     uint16_t* orow = a.out[tensor] + row * out_ld;
     if (tensor == 2) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      qkv_unit<LPH, U, false>(xrow, a.bias[2], orow, heads, lane, c, src, half, rot_chunks, z, z, a.eps);
+      qkv_unit<LPH, U, false, ILV>(xrow, a.bias[2], orow, heads, lane, c, src, half, rot_chunks, z, z, a.eps);
     } else {
       uint4 cw = make_uint4(0u, 0u, 0u, 0u), sw = make_uint4(0u, 0u, 0u, 0u);
       if (c < rot_chunks) {
         cw = load16_reused(a.cos + row * a.rot + c * 8);
         sw = load16_reused(a.sin + row * a.rot + c * 8);
       }
-      qkv_unit<LPH, U, true>(xrow, a.bias[tensor], orow, heads, lane, c, src, half, rot_chunks, cw, sw,
-                             a.eps);
+      qkv_unit<LPH, U, true, ILV>(xrow, a.bias[tensor], orow, heads, lane, c, src, half, rot_chunks, cw,
+                                  sw, a.eps);
     }
   }
 }
@@ -176,22 +190,33 @@ __global__ void __launch_bounds__(kThreads) qkv_epilogue_kernel(const QkvArgs a)
 // 256-thread blocks per SM).
 constexpr int kUnroll = 4;
 
-template <int LPH>
+template <int LPH, bool ILV>
 cudaError_t launch_lph(const QkvArgs& a, cudaStream_t stream) {
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&qkv_epilogue_kernel<LPH, kUnroll>),
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&qkv_epilogue_kernel<LPH, kUnroll, ILV>),
                                       kThreads, 0, (3 * a.rows + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
-  qkv_epilogue_kernel<LPH, kUnroll><<<blocks, kThreads, 0, stream>>>(a);
+  qkv_epilogue_kernel<LPH, kUnroll, ILV><<<blocks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <bool ILV>
+cudaError_t launch_ilv(const QkvArgs& a, int64_t head_dim, cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_lph<8, ILV>(a, stream);
+    case 128: return launch_lph<16, ILV>(a, stream);
+    case 256: return launch_lph<32, ILV>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
                                 const uint16_t* const bias[3], uint16_t* const out[3],
-                                const uint16_t* cos, const uint16_t* sin, int64_t rot, int64_t rows,
-                                int64_t heads, int64_t head_dim, float eps, cudaStream_t stream) {
+                                const uint16_t* cos, const uint16_t* sin, int64_t rot, int interleaved,
+                                int64_t rows, int64_t heads, int64_t head_dim, float eps,
+                                cudaStream_t stream) {
   QkvArgs a;
   for (int i = 0; i < 3; ++i) {
     a.x[i] = x[i];
@@ -202,16 +227,12 @@ cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
   a.cos = cos;
   a.sin = sin;
   a.rot = rot;
+  a.interleaved = interleaved;
   a.rows = rows;
   a.heads = heads;
   a.eps = eps;
   if (rows == 0) return cudaSuccess;
-  switch (head_dim) {
-    case 64: return launch_lph<8>(a, stream);
-    case 128: return launch_lph<16>(a, stream);
-    case 256: return launch_lph<32>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return interleaved ? launch_ilv<true>(a, head_dim, stream) : launch_ilv<false>(a, head_dim, stream);
 }
 
 }  // namespace h3q

@@ -37,7 +37,7 @@ def test_header_declares_the_four_calls():
 def test_every_declared_symbol_is_exported(lib):
     for fn in _declared_functions():
         assert hasattr(lib, fn), f"{fn} is declared in h3q.h but not exported"
-    assert lib.h3q_abi_version() == 1
+    assert lib.h3q_abi_version() == 2
 
 
 def _q(lib, x=0x10000, ld=256, rows=4, cols=256, gsf=0x20000, codes=0x30000, scales=0x40000):
@@ -190,12 +190,12 @@ def test_swiglu_packed_rejects_bad_arguments_on_the_host(lib):
 
 
 def test_qkv_epilogue_rejects_bad_arguments_on_the_host(lib):
-    # (q, ld_q, k, ld_k, v, ld_v, bias_q, bias_k, bias_v, cos, sin, rot, rows, heads, head_dim,
-    #  eps, q_out, k_out, v_out, stream): 8 rows of 2 heads of 128
-    names = ["q", "ld_q", "k", "ld_k", "v", "ld_v", "bq", "bk", "bv", "cos", "sin", "rot", "rows",
+    # (q, ld_q, k, ld_k, v, ld_v, bias_q, bias_k, bias_v, cos, sin, rot, interleaved, rows, heads,
+    #  head_dim, eps, q_out, k_out, v_out, stream): 8 rows of 2 heads of 128
+    names = ["q", "ld_q", "k", "ld_k", "v", "ld_v", "bq", "bk", "bv", "cos", "sin", "rot", "ilv", "rows",
              "heads", "hd", "eps", "qo", "ko", "vo", "stream"]
     good = [0x1000000, 256, 0x1100000, 256, 0x1200000, 256, 0x2000000, 0x2100000, 0x2200000,
-            0x3000000, 0x3100000, 64, 8, 2, 128, 1e-6, 0x4000000, 0x4100000, 0x4200000, None]
+            0x3000000, 0x3100000, 64, 0, 8, 2, 128, 1e-6, 0x4000000, 0x4100000, 0x4200000, None]
     f = lib.h3q_qkv_epilogue
 
     def call(**kw):
@@ -219,6 +219,7 @@ def test_qkv_epilogue_rejects_bad_arguments_on_the_host(lib):
     assert call(vo=0x1000000 + 256) == 1 and "overlap" in h3q.h3q_last_error()  # v_out inside q
     assert call(ko=0x4000000 + 4096 - 16) == 1 and "overlap" in h3q.h3q_last_error()  # k_out on q_out
     assert call(qo=0x3000000) == 1                                      # q_out on cos
+    assert call(ilv=1) in (0, 2) and call(ilv=2) == 1 and "interleaved" in h3q.h3q_last_error()
     assert call(rows=0, q=None, k=None, v=None) == h3q.H3Q_OK
 
 

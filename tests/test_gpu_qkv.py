@@ -23,15 +23,15 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _run(w):
+def _run(w, interleaved=False):
     rows = w["q"].shape[0]
     outs = [fill(torch.empty((rows, w["heads"], w["head_dim"]), dtype=torch.bfloat16,
                              device=w["q"].device)) for _ in range(3)]
     return h3q.h3q_qkv_epilogue(w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"],
-                                w["eps"], outs=outs)
+                                w["eps"], outs=outs, interleaved=interleaved)
 
 
-def _oracle(w, idx=None):
+def _oracle(w, idx=None, interleaved=False):
     """The oracle's q, k, v outputs (rows `idx` only, when given)."""
     def sel(t):
         if t is None:
@@ -42,7 +42,8 @@ def _oracle(w, idx=None):
     out = []
     for i, name in enumerate("qkv"):
         out.append(oracle.qkv_epilogue_rows(sel(w[name]), bits(w["biases"][i]), w["heads"], cos, sin,
-                                            w["eps"], is_v=(name == "v"), threads=THREADS))
+                                            w["eps"], is_v=(name == "v"), threads=THREADS,
+                                            interleaved=interleaved))
     return out
 
 
@@ -62,6 +63,24 @@ def test_shapes(dev, rows, heads, hd, rot, packed):
     w = workloads.qkv_inputs(dev, rows=rows, heads=heads, head_dim=hd, rot=rot, seed=rows + heads + rot,
                              packed=packed)
     _check(_run(w), _oracle(w), f"qkv {rows}x{heads}x{hd} rot {rot}")
+
+
+@pytest.mark.parametrize("rows,heads,hd,rot,packed", [
+    (1, 1, 128, 64, True), (37, 56, 128, 128, True), (41, 7, 64, 32, False), (17, 3, 256, 96, True),
+    (300, 24, 128, 16, True)])
+def test_interleaved_pairs(dev, rows, heads, hd, rot, packed):
+    """RoPE on the pairs (2j, 2j+1) (the FlashRT page's fused RMSNorm + RoPE kernel)."""
+    w = workloads.qkv_inputs(dev, rows=rows, heads=heads, head_dim=hd, rot=rot, seed=rows + 7 * heads,
+                             packed=packed)
+    _check(_run(w, interleaved=True), _oracle(w, interleaved=True), f"qkv interleaved {rows}x{heads}x{hd}")
+
+
+def test_full_workload_interleaved_sampled_rows(dev):
+    w = workloads.qkv_inputs(dev, seed=8)
+    got = _run(w, interleaved=True)
+    torch.cuda.synchronize()
+    idx = workloads.sample_rows(w["q"].shape[0], random=512).to(dev)
+    _check([g.index_select(0, idx) for g in got], _oracle(w, idx, interleaved=True), "qkv interleaved full")
 
 
 def test_eps_and_large_values(dev):
