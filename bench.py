@@ -529,7 +529,27 @@ def measure_producers(h3q, dev, stream, args):
             "gbs_at_full_issue": round(swiglu_bytes(*gate.shape) / (ms_issue * 1e-3) / 1e9, 1),
             "sm_mhz": args.sm_mhz_seen,
             "source": "ncu smsp__sass_thread_inst_executed.sum per element, profiles/inst_per_element.txt"}
-    del c, s
+    # dynamic SwiGLU step: abs-max pass, device global scale, producer
+    amax_s = torch.zeros(1, dtype=torch.float32, device=dev)
+    g_s = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def swiglu_dynamic_step():
+        amax_s.zero_()
+        h3q.h3q_swiglu_amax(gate, up, amax=amax_s, stream=stream)
+        h3q.h3q_global_scale_from_amax(amax_s, g_s, stream=stream)
+        h3q.h3q_swiglu_nvfp4(gate, up, g_s, c, s, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            swiglu_dynamic_step()
+    _, per = time_launches(swiglu_dynamic_step, n, stream)
+    sd = entry(swiglu_bytes(*gate.shape), per, gate.shape[0])
+    sd["two_pass_algorithmic_bytes"] = swiglu_bytes(*gate.shape) + 4 * gate.numel()
+    sd["frac_of_peak_two_pass"] = round(sd["two_pass_algorithmic_bytes"] / (sd["median_launch_ms"] * 1e-3) / 1e9
+                                        / peak, 4)
+    sd["note"] = "abs-max pass + device scale + producer; gate and up read twice, GB/s by the single-pass bytes"
+    res["swiglu_dynamic_scale_65280x18944"] = sd
+    del c, s, amax_s, g_s
 
     # SwiGLU of the value-first packed projection with its bias, 65,280 x 2 x 18,944
     del gate, up
@@ -552,6 +572,27 @@ def measure_producers(h3q, dev, stream, args):
             h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream)
         _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream)
         res[f"attn_out_quantize_{tokens}x7168"] = entry(quantize_bytes(*x.shape), per, tokens)
+        if tokens == 65280:
+            # the dynamic-scale quantize without caller scratch (abs-max pass, scale, quantize)
+            gd = torch.empty(1, dtype=torch.float32, device=dev)
+            for _ in range(3):
+                h3q.h3q_quantize_nvfp4_dynamic(x, gd, c, s, stream=stream)
+            _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4_dynamic(x, gd, c, s, stream=stream), n,
+                                   stream)
+            dq = entry(quantize_bytes(*x.shape), per, tokens)
+            dq["two_pass_algorithmic_bytes"] = quantize_bytes(*x.shape) + 2 * x.numel()
+            dq["frac_of_peak_two_pass"] = round(dq["two_pass_algorithmic_bytes"] / (dq["median_launch_ms"] * 1e-3)
+                                                / 1e9 / peak, 4)
+            dq["note"] = "abs-max pass + device scale + quantize in one call; GB/s by the single-pass bytes"
+            res["attn_out_quantize_dynamic_65280x7168"] = dq
+            # the checking-path dequantize of that output: codes + scales in, fp32 out
+            out = torch.empty(x.shape, dtype=torch.float32, device=dev)
+            for _ in range(3):
+                h3q.h3q_dequantize_nvfp4(c, s, g, out=out, stream=stream)
+            _, per = time_launches(lambda: h3q.h3q_dequantize_nvfp4(c, s, g, out=out, stream=stream), n, stream)
+            res["dequantize_65280x7168"] = entry(x.numel() // 2 + padded(tokens) * COLS // 16 + 4 * x.numel() + 4,
+                                                 per, tokens)
+            del out, gd
         del x, c, s
 
     # dynamic AdaLN: per-call abs-max pass, device global scale, producer (three
