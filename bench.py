@@ -509,7 +509,11 @@ def measure_producers(h3q, dev, stream, args):
                 "median_launch_ms": round(ms, 5), "rows_per_s": round(rows / (ms * 1e-3)),
                 "algorithmic_bytes": nbytes, "launches": len(per)}
 
+    # Each producer's inputs come from fresh device allocations (the caching
+    # allocator's blocks released first): the placement of a large strided tensor
+    # inside a reused segment can move a launch's time by several per cent.
     # SwiGLU 65,280 x 18,944 (5.6 GB per call: larger than L2)
+    torch.cuda.empty_cache()
     gate, up = workloads.swiglu_inputs(dev)
     g = torch.tensor([calibrate_swiglu_gsf(gate, up)], dtype=torch.float32, device=dev)
     c, s = h3q.h3q_swiglu_nvfp4(gate, up, g, stream=stream)
@@ -553,6 +557,7 @@ def measure_producers(h3q, dev, stream, args):
 
     # SwiGLU of the value-first packed projection with its bias, 65,280 x 2 x 18,944
     del gate, up
+    torch.cuda.empty_cache()
     o, bias = workloads.swiglu_packed_inputs(dev)
     c, s = h3q.h3q_swiglu_packed_nvfp4(o, g, bias=bias, stream=stream)
     for _ in range(3):
@@ -565,6 +570,7 @@ def measure_producers(h3q, dev, stream, args):
 
     # attention-output quantize: 65,280 and 300,000 tokens of 56 x 128
     for tokens in (65280, 300000):
+        torch.cuda.empty_cache()
         x = workloads.attention_output(dev, tokens=tokens)
         g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
         c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
@@ -598,6 +604,7 @@ def measure_producers(h3q, dev, stream, args):
     # dynamic AdaLN: per-call abs-max pass, device global scale, producer (three
     # launches and an fp32 zero fill per step, no host synchronisation); GB/s by the
     # single-pass algorithmic bytes, although x is read twice
+    torch.cuda.empty_cache()
     w = workloads.adaln_inputs(dev)
     amax = torch.zeros(1, dtype=torch.float32, device=dev)
     g = torch.empty(1, dtype=torch.float32, device=dev)
@@ -628,6 +635,7 @@ def measure_producers(h3q, dev, stream, args):
     del w, c, s
 
     # residual fold + RMSNorm + AdaLN: h (fp32) is read and written back each launch
+    torch.cuda.empty_cache()
     w = workloads.residual_inputs(dev)
     g = torch.tensor([90.0], dtype=torch.float32, device=dev)
     c = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
@@ -646,6 +654,7 @@ def measure_producers(h3q, dev, stream, args):
 
     # QKV epilogue: 65,280 tokens x 56 heads x 128 (ROT 64), q, k, v column slices of
     # one packed projection, bf16 [rows, heads, 128] outputs
+    torch.cuda.empty_cache()
     w = workloads.qkv_inputs(dev)
     outs = h3q.h3q_qkv_epilogue(w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"],
                                 w["eps"], stream=stream)
@@ -662,6 +671,7 @@ def measure_producers(h3q, dev, stream, args):
     del w, outs
 
     # standalone quantize 8,192 x 7,168 (150 MB: near L2, so L2 is flushed before each launch)
+    torch.cuda.empty_cache()
     x = workloads.quantize_inputs(dev)
     g = torch.tensor([2688.0 / float(x.float().abs().max())], dtype=torch.float32, device=dev)
     c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
