@@ -3,8 +3,11 @@
 // out = fl((E2M1value(c) * E4M3value(sf)) / gsf): the value a block-scaled
 // NVFP4 GEMM with alpha = 1/gsf sees for the element.  The product is exact
 // (2 x 4 significant bits), so there is one rounding, a correctly rounded
-// division.  One lane per 16-element block: an 8-byte code load, the scale
-// byte from its swizzled position, two 256-bit stores of fp32.
+// division.  The value depends only on the code and the scale byte, so each
+// CTA first tabulates it for all 16 codes x 128 scale values (8 KB of shared
+// memory, one division per entry) and an element is then a table load.  One
+// lane per 16-element block: an 8-byte code load, the scale byte from its
+// swizzled position, two 256-bit stores of fp32.
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
 
@@ -27,7 +30,14 @@ __global__ void __launch_bounds__(kThreads)
 dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                   int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
                   float* __restrict__ out) {
+  // tab[sf * 16 + c] = fl((E2M1value(c) * E4M3value(sf)) / gsf); the decode
+  // reads the scale byte's low seven bits (bit 7 is not part of the code)
+  __shared__ float tab[128 * 16];
   const float gsf = *gsf_ptr;
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x)
+    tab[i] = __fdiv_rn(__fmul_rn(e2m1_value(static_cast<uint32_t>(i & 15)),
+                                 e4m3_value(static_cast<uint32_t>(i >> 4))), gsf);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
   const int64_t quads = cols >> 6;
@@ -44,13 +54,10 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__
                  : "=r"(lo), "=r"(hi)
                  : "l"(codes + row * (cols >> 1) + g * 8));
     const uint32_t sf = scales[scale_word_offset(row, g >> 2, quads) + (g & 3)];
-    const float sfv = e4m3_value(sf);
+    const float* row_tab = tab + (sf & 0x7fu) * 16;
     float v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t c = ((i < 8 ? lo : hi) >> (4 * (i & 7))) & 15u;
-      v[i] = __fdiv_rn(__fmul_rn(e2m1_value(c), sfv), gsf);
-    }
+    for (int i = 0; i < 16; ++i) v[i] = row_tab[((i < 8 ? lo : hi) >> (4 * (i & 7))) & 15u];
     float* o = out + row * cols + g * kBlock;
     asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(o), "f"(v[0]),
                  "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
