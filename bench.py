@@ -873,6 +873,14 @@ def run_single(args, dev):
             w["h"], w["o"], w["gate"], w["gamma"], w["table"], g, bias=w["bias"], rows_per_frame=RPF,
             eps=w["eps"], codes=c, scales=s, stream=stream)
         nbytes = residual_bytes(rows, COLS, w["table"].shape[0])
+    elif kind == "dequantize":
+        rows = args.rows or ROWS
+        x = workloads.attention_output(dev, tokens=rows)
+        g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
+        c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
+        out = torch.empty(x.shape, dtype=torch.float32, device=dev)
+        fn = lambda: h3q.h3q_dequantize_nvfp4(c, s, g, out=out, stream=stream)  # noqa: E731
+        nbytes = rows * COLS // 2 + padded(rows) * COLS // 16 + 4 * rows * COLS + 4
     elif kind == "qkv":
         rows = args.rows or ROWS
         w = workloads.qkv_inputs(dev, rows=rows)
@@ -914,7 +922,8 @@ def main(argv=None):
     p.add_argument("--reference-rows", type=int, default=510)
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--kernel", choices=["adaln", "swiglu", "swiglu_packed", "quantize", "residual", "qkv"],
+    p.add_argument("--kernel", choices=["adaln", "swiglu", "swiglu_packed", "quantize", "residual", "qkv",
+                                        "dequantize"],
                    help="time one producer alone (for profiling); prints a short JSON line")
     p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)
