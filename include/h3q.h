@@ -146,7 +146,9 @@ int h3q_quantize_nvfp4(const void *x, int64_t ld_x, int64_t rows, int64_t cols,
  *                   row with an out-of-range entry is unspecified.
  *   rows_per_frame  used when row_frame is NULL: frame = row / rows_per_frame;
  *                   must be >= 1 with (rows-1)/rows_per_frame < num_frames.
- *   eps             finite, >= 0.
+ *   eps             finite, >= 0.  With eps = 0 a row whose sum of squares is 0 has
+ *                   rstd = 1/0 = +inf and NaN values (0 * inf); its codes and scales
+ *                   are then unspecified, like those of NaN or infinite inputs.
  *   row_rstd        optional out fp32 [rows]: rstd of each row, or NULL.
  */
 int h3q_rmsnorm_adaln_nvfp4(const void *x, int64_t ld_x, const void *gamma,
@@ -318,7 +320,8 @@ int h3q_quantize_nvfp4_dynamic(const void *x, int64_t ld_x, int64_t rows, int64_
  *   rot            ROT, a multiple of 16 with 0 <= rot <= head_dim.
  *   interleaved    0: rotate-half pairs (i, i + ROT/2); 1: pairs (2j, 2j + 1).
  *   heads          H >= 1; head_dim HD in {64, 128, 256}; heads * head_dim <= 2^24.
- *   eps            finite, >= 0.
+ *   eps            finite, >= 0 (with eps = 0 an all-zero head gives NaN values, whose
+ *                  bit patterns are unspecified).
  *   q_out, k_out, v_out  bf16 [rows, heads, head_dim] contiguous, 16-byte
  *                  aligned, caller-owned; they must not overlap an input or
  *                  each other.

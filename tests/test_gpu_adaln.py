@@ -180,3 +180,17 @@ def test_repeated_unsynchronised(dev):
                                      w["eps"], float(gsf.item()), threads=THREADS)
     for codes, scales in outs:
         check_full(codes, scales, 1024, 7168, co, so, "adaln repeat")
+
+
+def test_maximum_width(dev):
+    """Rows of 2^24 columns, the widest the ABI accepts (the generic kernel: x read
+    twice, tables per row)."""
+    rows, cols = 2, 1 << 24
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=1, rows_per_frame=rows, seed=77)
+    frames = np.zeros(rows, np.int64)
+    gsf = _oracle_gsf(w, frames)
+    codes, scales, rstd = _run(dev, w, gsf, rows_per_frame=rows)
+    co, so, ro, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                      gsf, threads=THREADS)
+    check_full(codes, scales, rows, cols, co, so, "adaln 2 x 2^24")
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), ro.view(np.uint32))

@@ -171,3 +171,12 @@ def test_outputs_do_not_spill_past_their_buffers(dev):
     assert (cbuf[nc:] == 0xAB).all() and (sbuf[ns:] == 0xAB).all()
     co, so = oracle.quantize_rows(bits(x), gsf)
     check_full(codes, scales, rows, cols, co, so, "guarded quantize")
+
+
+def test_quantize_maximum_width(dev):
+    """Rows of 2^24 columns, the widest the ABI accepts."""
+    x = workloads.quantize_inputs(dev, rows=3, cols=1 << 24, seed=78)
+    g = oracle.global_scale(float(x.float().abs().max()))
+    codes, scales = h3q.h3q_quantize_nvfp4(x, gsf_tensor(g, dev))
+    co, so = oracle.quantize_rows(bits(x), g, threads=THREADS)
+    check_full(codes, scales, 3, 1 << 24, co, so, "quantize 3 x 2^24")
