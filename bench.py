@@ -402,10 +402,11 @@ def run_ours(args, rank, world, dev):
 
 
 def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
-    """The same metric through the public host-buffer call: each step copies x,
-    gamma and the modulation table from pinned host memory, runs the producer and
-    copies codes and scales back to pinned host memory.  The call pipelines the
-    copies and the producer over 8,192-row chunks on three streams; the timed
+    """The same metric through the C-ABI host-buffer call (h3q_rmsnorm_adaln_nvfp4_host,
+    through HostPipeline): each step copies gamma and the modulation table from pinned
+    host memory to the device, then the call copies x in, runs the producer and copies
+    codes and scales back to pinned host memory, pipelined over 8,192-row chunks (the
+    producer on the caller's stream, a library stream per copy direction).  The timed
     region (CUDA events on the caller's stream) covers every copy of the step."""
     from nvfp4_activation_quantize_gb300.host import HostPipeline
 
@@ -436,6 +437,7 @@ def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
         "d2h_bytes_per_step": d2h,
         "steps": steps,
         "ms_per_step": round(total_ms / steps, 3),
+        "call": "h3q_rmsnorm_adaln_nvfp4_host",
         "pipeline": {"chunk_rows": pipe.chunk_rows, "depth": pipe.depth, "streams": 3},
         "check": e2e_matches(h3q, dev, w, gsf, hc, hs),
     }

@@ -88,6 +88,19 @@ static inline int64_t h3q_scale_bytes(int64_t rows, int64_t cols)
 {
     return h3q_padded_rows(rows) * (cols / 16);
 }
+/* n rounded up to a multiple of 256 bytes. */
+static inline int64_t h3q_align256(int64_t n) { return (n + 255) / 256 * 256; }
+/* Device workspace of h3q_rmsnorm_adaln_nvfp4_host: three staging slots of
+ * chunk_rows rows, each an x chunk, a code chunk and a scale chunk (each part
+ * rounded up to 256 bytes, in that order), then -- when the frames come from
+ * rows_per_frame (with_frames != 0) -- the rows' frame indices, rows int32. */
+static inline int64_t h3q_host_workspace_bytes(int64_t chunk_rows, int64_t cols, int64_t rows,
+                                               int with_frames)
+{
+    int64_t slot = h3q_align256(chunk_rows * cols * 2) + h3q_align256(chunk_rows * cols / 2) +
+                   h3q_align256(chunk_rows * cols / 16);
+    return 3 * slot + (with_frames ? h3q_align256(rows * 4) : 0);
+}
 /* Bytes of the packed code matrix. */
 static inline int64_t h3q_code_bytes(int64_t rows, int64_t cols) { return rows * (cols / 2); }
 /* Byte offset, in the scale matrix, of the scales of row `row0` onwards when
@@ -332,6 +345,42 @@ int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, c
                      const void *cos, const void *sin, int64_t rot, int interleaved, int64_t rows,
                      int64_t heads, int64_t head_dim, float eps, void *q_out, void *k_out,
                      void *v_out, void *stream);
+
+/*
+ * h3q_rmsnorm_adaln_nvfp4 on HOST buffers: x read from host memory, codes and
+ * scales written to host memory, the copies inside the call.  The rows are cut
+ * into chunks of chunk_rows rows (a multiple of 128); the producer runs on the
+ * caller's stream on chunk i while a library stream copies chunk i+1 in and
+ * another copies chunk i-1's codes and scales out (the scales of a 128-row tile
+ * are one contiguous range, h3q_scale_offset_of_row_tile).  The outputs equal
+ * h3q_rmsnorm_adaln_nvfp4's byte for byte.
+ *
+ *   x_host          bf16 [rows, cols], contiguous, in host memory (page-locked
+ *                   for the copies to run asynchronously and overlap).
+ *   codes_host      out, host uint8 [rows, cols/2], contiguous.
+ *   scales_host     out, host uint8 [h3q_padded_rows(rows), cols/16], contiguous.
+ *   gamma, mod_table, num_frames, row_frame, rows_per_frame, eps, global_scale:
+ *                   as h3q_rmsnorm_adaln_nvfp4, in device memory (row_frame
+ *                   int32 [rows] or NULL).
+ *   workspace       device memory of at least h3q_host_workspace_bytes(chunk_rows,
+ *                   cols, rows, row_frame == NULL) bytes, 256-byte aligned, owned
+ *                   by the caller and not touched by other work until the stream
+ *                   has passed this call.
+ *   chunk_rows      a positive multiple of 128.
+ * Ordering: the call runs after the work queued on `stream` before it, and work
+ * queued on `stream` after it starts after its last copy back, so the host
+ * outputs may be read once `stream` has been synchronised.  On its first call on
+ * a device the library creates two non-blocking streams and a few events for
+ * that device and keeps them; it allocates no memory.  Calls on one device are
+ * enqueued one at a time (a lock), and stay asynchronous.  Status codes as the
+ * other calls; a failure after the first copy was queued leaves the outputs
+ * unspecified.
+ */
+int h3q_rmsnorm_adaln_nvfp4_host(const void *x_host, int64_t rows, int64_t cols, const void *gamma,
+                                 const void *mod_table, int64_t num_frames, const int32_t *row_frame,
+                                 int64_t rows_per_frame, float eps, const float *global_scale,
+                                 uint8_t *codes_host, uint8_t *scales_host, void *workspace,
+                                 int64_t workspace_bytes, int64_t chunk_rows, void *stream);
 
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char *h3q_last_error(void);

@@ -24,7 +24,7 @@ __all__ = [
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
     "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
-    "h3q_qkv_epilogue",
+    "h3q_qkv_epilogue", "h3q_rmsnorm_adaln_nvfp4_host", "host_workspace_bytes",
 ]
 
 H3Q_OK = 0
@@ -47,6 +47,8 @@ _SIGNATURES = {
     "h3q_swiglu_packed_nvfp4": [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P],
     "h3q_residual_rmsnorm_adaln_nvfp4": [_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _I64,
                                          ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P],
+    "h3q_rmsnorm_adaln_nvfp4_host": [_P, _I64, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _P, _P, _P, _P,
+                                     _I64, _I64, _P],
     "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _I64, _I64,
                          _I64, ctypes.c_float, _P, _P, _P, _P],
 }
@@ -104,6 +106,14 @@ def padded_rows(rows: int) -> int:
 
 def scale_bytes(rows: int, cols: int) -> int:
     return padded_rows(rows) * (cols // 16)
+
+
+def host_workspace_bytes(chunk_rows: int, cols: int, rows: int, with_frames: bool) -> int:
+    """Device workspace bytes of h3q_rmsnorm_adaln_nvfp4_host (h3q_host_workspace_bytes in
+    include/h3q.h): three staging slots, then the frames when they come from rows_per_frame."""
+    a = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    slot = a(chunk_rows * cols * 2) + a(chunk_rows * cols // 2) + a(chunk_rows * cols // 16)
+    return 3 * slot + (a(rows * 4) if with_frames else 0)
 
 
 def _check(fn: str, rc: int) -> None:
@@ -490,3 +500,47 @@ def h3q_qkv_epilogue(q, k, v, biases, cos, sin, heads, eps, outs=None, interleav
                                         outs[1].data_ptr(), outs[2].data_ptr(), _stream(stream, dev))
     _check("h3q_qkv_epilogue", rc)
     return outs[0], outs[1], outs[2]
+
+
+def h3q_rmsnorm_adaln_nvfp4_host(x_host, gamma, mod_table, global_scale, codes_host, scales_host, workspace, *,
+                                 row_frame=None, rows_per_frame=None, eps=1e-6, chunk_rows=8192, stream=None):
+    """RMSNorm + AdaLN -> NVFP4 on host buffers: x_host (contiguous bf16 [rows, cols] in
+    host memory, pinned for the copies to overlap) into host codes [rows, cols/2] and
+    scales [pad128(rows), cols/16] (uint8, contiguous), the copies inside the library
+    call, pipelined over `chunk_rows`-row chunks.  gamma, mod_table, global_scale and
+    row_frame are CUDA tensors; `workspace` is a CUDA uint8 tensor of at least
+    host_workspace_bytes(chunk_rows, cols, rows, row_frame is None) bytes.  The host
+    outputs may be read once `stream` (default: the current stream) is synchronised."""
+    import torch
+
+    if not isinstance(x_host, torch.Tensor) or x_host.is_cuda or x_host.dtype != torch.bfloat16:
+        raise ValueError("x_host must be a host bf16 tensor")
+    if x_host.dim() != 2 or not x_host.is_contiguous():
+        raise ValueError("x_host must be contiguous [rows, cols]")
+    rows, cols = x_host.shape
+    _cuda_tensor("workspace", workspace, torch.uint8)
+    dev = workspace.device
+    for name, t, shape in (("codes_host", codes_host, (rows, cols // 2)),
+                           ("scales_host", scales_host, (padded_rows(rows), cols // 16))):
+        if (not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.uint8 or tuple(t.shape) != shape
+                or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host uint8 tensor {shape}")
+    _contiguous("gamma", gamma, torch.bfloat16, (cols,), dev)
+    _cuda_tensor("mod_table", mod_table, torch.bfloat16, dev)
+    if mod_table.dim() != 3 or mod_table.shape[1:] != (2, cols) or not mod_table.is_contiguous():
+        raise ValueError("mod_table must be contiguous [frames, 2, cols]")
+    rf_ptr = None
+    if row_frame is not None:
+        _contiguous("row_frame", row_frame, torch.int32, (rows,), dev)
+        rf_ptr = row_frame.data_ptr()
+        rows_per_frame = 0
+    elif rows_per_frame is None:
+        raise ValueError("give row_frame or rows_per_frame")
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_rmsnorm_adaln_nvfp4_host(
+            x_host.data_ptr(), rows, cols, gamma.data_ptr(), mod_table.data_ptr(), mod_table.shape[0], rf_ptr,
+            int(rows_per_frame), float(eps), gsf.data_ptr(), codes_host.data_ptr(), scales_host.data_ptr(),
+            workspace.data_ptr(), workspace.numel(), int(chunk_rows), _stream(stream, dev))
+    _check("h3q_rmsnorm_adaln_nvfp4_host", rc)
+    return codes_host, scales_host

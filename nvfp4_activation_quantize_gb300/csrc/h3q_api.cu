@@ -513,4 +513,52 @@ int h3q_qkv_epilogue(const void* q, int64_t ld_q, const void* k, int64_t ld_k, c
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_rmsnorm_adaln_nvfp4_host(const void* x_host, int64_t rows, int64_t cols, const void* gamma,
+                                 const void* mod_table, int64_t num_frames, const int32_t* row_frame,
+                                 int64_t rows_per_frame, float eps, const float* global_scale,
+                                 uint8_t* codes_host, uint8_t* scales_host, void* workspace,
+                                 int64_t workspace_bytes, int64_t chunk_rows, void* stream) {
+  static const char* fn = "h3q_rmsnorm_adaln_nvfp4_host";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (!std::isfinite(eps) || eps < 0.0f) return invalid(fn, "eps must be finite and >= 0");
+  if (num_frames < 1) return invalid(fn, "num_frames must be >= 1");
+  if (num_frames > (int64_t(1) << 31)) return invalid(fn, "num_frames exceeds 2^31");
+  if (chunk_rows <= 0 || chunk_rows % 128 != 0) return invalid(fn, "chunk_rows must be a positive multiple of 128");
+  if (chunk_rows > (int64_t(1) << 40) / cols) return invalid(fn, "chunk_rows * cols is too large");
+  if (rows == 0) return H3Q_OK;
+  if (x_host == nullptr || codes_host == nullptr || scales_host == nullptr)
+    return invalid(fn, "x_host, codes_host and scales_host must not be NULL");
+  if (int e = check_input(fn, "gamma", gamma, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "mod_table", mod_table, cols, 2 * num_frames, cols)) return e;
+  if (global_scale == nullptr || !aligned(global_scale, 4))
+    return invalid(fn, "global_scale must be a 4-byte aligned pointer");
+  if (row_frame != nullptr) {
+    if (!aligned(row_frame, 4)) return invalid(fn, "row_frame must be 4-byte aligned");
+  } else {
+    if (rows_per_frame < 1) return invalid(fn, "rows_per_frame must be >= 1 when row_frame is NULL");
+    if ((rows - 1) / rows_per_frame >= num_frames)
+      return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
+  }
+  if (workspace == nullptr || !aligned(workspace, 256)) return invalid(fn, "workspace must be 256-byte aligned");
+  if (workspace_bytes < h3q_host_workspace_bytes(chunk_rows, cols, rows, row_frame == nullptr))
+    return invalid(fn, "workspace_bytes is below h3q_host_workspace_bytes");
+  const Span xs = span(x_host, rows * cols * 2);
+  const Span c = span(codes_host, h3q_code_bytes(rows, cols));
+  const Span s = span(scales_host, h3q_scale_bytes(rows, cols));
+  if (overlap(xs, c) || overlap(xs, s) || overlap(c, s))
+    return invalid(fn, "host outputs overlap the input or each other");
+  const Span ws = span(workspace, workspace_bytes);
+  const Span dev_ins[4] = {span(gamma, cols * 2), span(mod_table, num_frames * 4 * cols),
+                           span(global_scale, 4), row_frame ? span(row_frame, rows * 4) : Span{0, 0}};
+  for (const Span& in : dev_ins)
+    if (overlap(in, ws)) return invalid(fn, "workspace overlaps a device input");
+  cudaError_t err = h3q::launch_adaln_host(
+      static_cast<const uint16_t*>(x_host), rows, cols, static_cast<const uint16_t*>(gamma),
+      static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, eps, global_scale,
+      codes_host, scales_host, static_cast<uint8_t*>(workspace), chunk_rows,
+      static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 }  // extern "C"

@@ -76,4 +76,14 @@ cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
                                 int64_t rows, int64_t heads, int64_t head_dim, float eps,
                                 cudaStream_t stream);
 
+// RMSNorm + AdaLN -> NVFP4 on host buffers (x in, codes and scales out), the
+// copies pipelined with the producer over chunk_rows-row chunks; `workspace`
+// holds h3q_host_workspace_bytes(chunk_rows, cols, rows, row_frame == nullptr)
+// bytes of device memory (include/h3q.h), 256-byte aligned.
+cudaError_t launch_adaln_host(const uint16_t* x_host, int64_t rows, int64_t cols, const uint16_t* gamma,
+                              const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
+                              int64_t rows_per_frame, float eps, const float* gsf, uint8_t* codes_host,
+                              uint8_t* scales_host, uint8_t* workspace, int64_t chunk_rows,
+                              cudaStream_t stream);
+
 }  // namespace h3q

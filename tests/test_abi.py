@@ -230,3 +230,30 @@ def test_python_binding_of_the_qkv_epilogue_refuses_host_tensors():
     b = torch.zeros(256, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         h3q.h3q_qkv_epilogue(x, x, x, (b, b, b), None, None, 2, 1e-6)
+
+
+def test_host_call_rejects_bad_arguments_on_the_host(lib):
+    # (x_host, rows, cols, gamma, table, frames, row_frame, rpf, eps, gsf, codes_host, scales_host,
+    #  workspace, workspace_bytes, chunk_rows, stream)
+    names = ["x", "rows", "cols", "gamma", "table", "frames", "rf", "rpf", "eps", "gsf", "codes", "scales",
+             "ws", "wsb", "chunk", "stream"]
+    need = h3q.host_workspace_bytes(256, 512, 1000, True)
+    good = [0x7000000, 1000, 512, 0x1000000, 0x1100000, 4, None, 250, 1e-6, 0x1200000, 0x7100000,
+            0x7200000, 0x2000000, need, 256, None]
+    f = lib.h3q_rmsnorm_adaln_nvfp4_host
+
+    def call(**kw):
+        a = list(good)
+        for name, value in kw.items():
+            a[names.index(name)] = value
+        return f(*a)
+
+    assert call() in (0, 2)
+    assert call(chunk=200) == 1 and "chunk_rows" in h3q.h3q_last_error()
+    assert call(wsb=need - 1) == 1 and "workspace" in h3q.h3q_last_error()
+    assert call(ws=0x2000010) == 1                                    # workspace not 256-byte aligned
+    assert call(x=None) == 1
+    assert call(rpf=200) == 1 and "modulation table" in h3q.h3q_last_error()
+    assert call(codes=0x7000000 + 4096) == 1 and "overlap" in h3q.h3q_last_error()  # codes inside x
+    assert call(ws=0x1000000 - 512) == 1 and "workspace" in h3q.h3q_last_error()      # workspace on gamma
+    assert call(rows=0, x=None) == h3q.H3Q_OK

@@ -1,5 +1,6 @@
-"""The pipelined host-buffer call of the RMSNorm + AdaLN -> NVFP4 producer: pinned
-host inputs and outputs, chunks of 128-row multiples on three streams.  Its
+"""The host-buffer call of the RMSNorm + AdaLN -> NVFP4 producer
+(h3q_rmsnorm_adaln_nvfp4_host, through HostPipeline): pinned host inputs and
+outputs, chunks of 128-row multiples, the copies inside the library call.  Its
 outputs must equal the oracle's byte for byte (small cases) and the single
 device-buffer call's (the 65,280 x 7,168 workload)."""
 import numpy as np
@@ -35,18 +36,19 @@ def _gsf(w, frames):
     return oracle.global_scale(float(np.abs(oracle.bf16_value(y)).max()))
 
 
-@pytest.mark.parametrize("rows,cols,rpf,chunk,depth", [
-    (300, 1024, 100, 128, 2),     # ragged last chunk (44 rows), frames across chunk edges
-    (1000, 2048, 77, 256, 3),     # more chunks than slots
-    (128, 512, 128, 128, 1),      # one chunk, one slot
-    (5, 7168, 2, 8192, 3),        # fewer rows than a tile
+@pytest.mark.parametrize("rows,cols,rpf,chunk", [
+    (300, 1024, 100, 128),     # ragged last chunk (44 rows), frames across chunk edges
+    (1000, 2048, 77, 256),     # more chunks than slots
+    (128, 512, 128, 128),      # one chunk
+    (5, 7168, 2, 8192),        # fewer rows than a tile
+    (1300, 640, 1300, 128),    # eleven chunks through three slots
 ])
-def test_matches_oracle(dev, rows, cols, rpf, chunk, depth):
+def test_matches_oracle(dev, rows, cols, rpf, chunk):
     w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=(rows + rpf - 1) // rpf,
                                rows_per_frame=rpf, seed=rows + cols)
     frames = np.arange(rows) // rpf
     gsf = _gsf(w, frames)
-    pipe = HostPipeline(dev, max_cols=cols + 64 * (depth - 1), chunk_rows=chunk, depth=depth)
+    pipe = HostPipeline(dev, max_cols=cols, chunk_rows=chunk)
     hc, hs = _host_outputs(rows, cols)
     hx = w["x"].cpu().pin_memory()
     pipe.rmsnorm_adaln_nvfp4(hx, w["gamma"].cpu(), w["table"].cpu(), gsf_tensor(gsf, "cpu"), hc, hs,
@@ -59,7 +61,7 @@ def test_matches_oracle(dev, rows, cols, rpf, chunk, depth):
 
 def test_host_row_frame_and_reuse(dev):
     """A host row_frame array, then the same pipeline reused for another shape."""
-    pipe = HostPipeline(dev, max_cols=4096, chunk_rows=256, depth=2)
+    pipe = HostPipeline(dev, max_cols=4096, chunk_rows=256)
     for rows, cols, seed in ((700, 4096, 1), (513, 1024, 2)):
         w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=6, seed=seed)
         rf = torch.randint(0, 6, (rows,), generator=torch.Generator().manual_seed(seed),
@@ -95,7 +97,7 @@ def test_full_65280x7168_equals_device_call(dev):
 
 
 def test_rejects_bad_shapes(dev):
-    pipe = HostPipeline(dev, max_cols=256, chunk_rows=128, depth=1)
+    pipe = HostPipeline(dev, max_cols=256, chunk_rows=128)
     x = torch.zeros((10, 512), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="max_cols"):
         pipe.rmsnorm_adaln_nvfp4(x, None, None, None, *_host_outputs(10, 512), rows_per_frame=1)

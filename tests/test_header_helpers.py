@@ -64,3 +64,32 @@ def test_row_tiles_are_contiguous_ranges(rows, cols):
         lo, hi = scale_offset_of_row_tile(r0, cols), scale_offset_of_row_tile(r1, cols)
         assert offs.min() == lo and offs.max() == hi - 1
         assert np.unique(offs).size == hi - lo
+
+
+WORKSPACE_PROGRAM = r"""
+#include <stdio.h>
+#include <inttypes.h>
+#include "h3q.h"
+int main(void) {
+    int64_t chunk, cols, rows, frames;
+    while (scanf("%" SCNd64 " %" SCNd64 " %" SCNd64 " %" SCNd64, &chunk, &cols, &rows, &frames) == 4)
+        printf("%" PRId64 "\n", h3q_host_workspace_bytes(chunk, cols, rows, (int)frames));
+    return 0;
+}
+"""
+
+
+def test_host_workspace_bytes_header_and_python_agree(tmp_path):
+    from nvfp4_activation_quantize_gb300 import host_workspace_bytes
+
+    src, exe = tmp_path / "w.c", tmp_path / "w"
+    src.write_text(WORKSPACE_PROGRAM)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe)], check=True)
+    cases = [(128, 64, 1, 1), (8192, 7168, 65280, 1), (8192, 7168, 65280, 0), (256, 1088, 1000, 1),
+             (384, 18944, 5, 0)]
+    out = subprocess.run([str(exe)], input="".join(f"{c} {k} {r} {f}\n" for c, k, r, f in cases),
+                         capture_output=True, text=True, check=True).stdout.split()
+    assert [int(v) for v in out] == [host_workspace_bytes(c, k, r, bool(f)) for c, k, r, f in cases]
+    # three slots of x, codes and scales (each rounded up to 256 bytes), then the frames
+    assert host_workspace_bytes(8192, 7168, 65280, True) == 3 * (8192 * 7168 * (2 + 0.5 + 1 / 16)) + 65280 * 4
