@@ -41,7 +41,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 2;
+// Segments in flight per warp: two for gate and up; one for the packed
+// projection with its bias, whose extra bias loads and adds would otherwise cost
+// the registers of a fourth CTA per SM (52 registers instead of 64).
+constexpr int kUnrollPlain = 2;
 
 constexpr float kL2E = 0x1.715476p+0f;    // fl(1 / ln 2)
 constexpr float kC1 = 0x1.62e430p-1f;     // fl(ln 2)
@@ -200,6 +203,7 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
               int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ amax,
               const uint16_t* __restrict__ bias_gate, const uint16_t* __restrict__ bias_up) {
+  constexpr int kUnroll = BIAS ? 1 : kUnrollPlain;
   __shared__ float inv_table[128];
   __shared__ __align__(16) float silu_table[2 * kTabHalf];
   const float gsf = AMAX ? 0.0f : *gsf_ptr;
