@@ -22,8 +22,8 @@
 // s = fl(g * sigma) depends on the bf16 gate alone, so -- as the pages' fused
 // SwiGLU producer does with its SiLU table (FastVideo API page,
 // swiglu_quantize) -- each CTA first tabulates s for every bf16 gate with
-// 2^-25 <= |g| <= 87 (8,030 values, 32 KB of shared memory), computed with the
-// arithmetic above.  A warp whose gates all lie in that range looks s up and
+// 2^-25 <= |g| <= 127.5 (8,192 values, 32 KB of shared memory), computed with
+// the arithmetic below.  A warp whose gates all lie in that range looks s up and
 // only forms y = bf16(fl(s * u)); other warps compute s directly.  Both give
 // the same bits.
 //
@@ -59,17 +59,16 @@ constexpr float kRound = 0x1.8p+23f;      // 1.5 * 2^23
 constexpr float kFastLimit = 87.0f;       // |z| <= 87: k in [-126, 127]
 
 // SiLU products s(g) = fl(g * sigma(g)) of the bf16 gates with magnitude bits in
-// [kTabLo, kTabHi] (2^-25 <= |g| <= 87), both signs, tabulated per CTA in shared
-// memory: entry sign * 4096 + (magnitude bits - kTabLo).
-constexpr uint32_t kTabLo = 0x3300u;  // bf16 bits of 2^-25
-constexpr uint32_t kTabHi = 0x42aeu;  // bf16 bits of 87
+// [kTabLo, kTabLo + 4095] (2^-25 <= |g| <= 127.5), both signs, tabulated per CTA
+// in shared memory: entry sign * 4096 + (magnitude bits - kTabLo).  With exactly
+// 4096 magnitudes a gate pair is inside the window iff w - (kTabLo, kTabLo) has
+// bits 12..14 of both halves clear (a magnitude below kTabLo borrows into them,
+// one above kTabLo + 4095 carries into them), so the window test is one AND per
+// pair.
+constexpr uint32_t kTabLo = 0x3300u;          // bf16 bits of 2^-25
+constexpr uint32_t kTabWord = kTabLo | (kTabLo << 16);
+constexpr uint32_t kTabOut = 0x70007000u;     // bits 12..14 of both halves
 constexpr int kTabHalf = 4096;
-
-__device__ __forceinline__ uint32_t absmin_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
 
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
@@ -139,48 +138,54 @@ __device__ __forceinline__ void swiglu_block(const Block16& g, const Block16& u,
 }
 
 // Byte offsets in the table of the gates in the low and high halves of a bf16 pair
-// whose magnitudes lie in [kTabLo, kTabHi]: w - (kTabLo, kTabLo) leaves
-// sign * 0x8000 + (magnitude - kTabLo) in each half without a borrow.
-__device__ __forceinline__ void table_offsets(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t d = w - (kTabLo | (kTabLo << 16));
+// inside the window, from d = w - kTabWord = sign * 0x8000 + (magnitude - kTabLo)
+// in each half (no borrow inside the window).
+__device__ __forceinline__ void table_offsets(uint32_t d, uint32_t& lo, uint32_t& hi) {
   lo = ((d << 2) & 0x3ffcu) | ((d >> 1) & 0x4000u);
   hi = ((d >> 14) & 0x3ffcu) | ((d >> 17) & 0x4000u);
 }
 
-__device__ __forceinline__ void swiglu_block_table(const Block16& g, const Block16& u, Block16& y,
+__device__ __forceinline__ void swiglu_block_table(const uint32_t (&d)[8], const Block16& u, Block16& y,
                                                    const char* table) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     uint32_t lo, hi;
-    table_offsets(g.w[i], lo, hi);
+    table_offsets(d[i], lo, hi);
     const float2 sv = make_float2(*reinterpret_cast<const float*>(table + lo),
                                   *reinterpret_cast<const float*>(table + hi));
     y.w[i] = float2_to_bf16x2(mul2(sv, bf16x2_to_float2_fma(u.w[i])));
   }
 }
 
-// Every gate of the block has magnitude in [kTabLo, kTabHi].
-__device__ __forceinline__ bool in_table(const Block16& g) {
-  const uint32_t mx = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(g.w[0], g.w[1]), absmax_bf16x2(g.w[2], g.w[3])),
-                                    absmax_bf16x2(absmax_bf16x2(g.w[4], g.w[5]), absmax_bf16x2(g.w[6], g.w[7])));
-  const uint32_t mn = absmin_bf16x2(absmin_bf16x2(absmin_bf16x2(g.w[0], g.w[1]), absmin_bf16x2(g.w[2], g.w[3])),
-                                    absmin_bf16x2(absmin_bf16x2(g.w[4], g.w[5]), absmin_bf16x2(g.w[6], g.w[7])));
-  const uint32_t mx_lo = mx & 0x7fffu, mx_hi = (mx >> 16) & 0x7fffu;
-  const uint32_t mn_lo = mn & 0x7fffu, mn_hi = (mn >> 16) & 0x7fffu;
-  return max(mx_lo, mx_hi) <= kTabHi && min(mn_lo, mn_hi) >= kTabLo;
+// The block's table words d_i = w_i - kTabWord; true when every gate of the
+// block lies inside the window.
+__device__ __forceinline__ bool table_words(const Block16& g, uint32_t (&d)[8]) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    d[i] = g.w[i] - kTabWord;
+    out |= d[i] & kTabOut;
+  }
+  return out == 0;
 }
 
 // Fill the table: entries i and i + kTabHalf hold the positive and negative gate
-// of magnitude bits kTabLo + i (computed as a pair, the FAST exponential: |g| <= 87).
+// of magnitude bits kTabLo + i, computed as a pair exactly as the direct path
+// computes them: the FAST exponential up to |g| = 87, the general one above.
 __device__ __forceinline__ void fill_silu_table(float* table) {
+  constexpr uint32_t kFastHi = 0x42aeu;  // bf16 bits of 87 (kFastLimit)
   for (int i = threadIdx.x; i < kTabHalf; i += blockDim.x) {
     const uint32_t mag = kTabLo + static_cast<uint32_t>(i);
-    if (mag > kTabHi) continue;
     const uint32_t pair = mag | ((mag | 0x8000u) << 16);  // (+g, -g)
     const float2 gv = bf16x2_to_float2(pair);
-    const float2 e = exp_neg2<true>(gv);
-    const float2 d = add2(splat(1.0f), e);
-    const float2 sv = mul2(gv, rcp_rn_ge1(d));
+    float2 sv;
+    if (mag <= kFastHi) {
+      const float2 d = add2(splat(1.0f), exp_neg2<true>(gv));
+      sv = mul2(gv, rcp_rn_ge1(d));
+    } else {
+      const float2 d = add2(splat(1.0f), exp_neg2<false>(gv));
+      sv = mul2(gv, make_float2(__frcp_rn(d.x), __frcp_rn(d.y)));
+    }
     table[i] = sv.x;
     table[i + kTabHalf] = sv.y;
   }
@@ -261,8 +266,9 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
         add_bias(ub[u], b);
       }
       Block16 y;
-      if (__all_sync(0xffffffffu, in_table(gb[u]))) {
-        swiglu_block_table(gb[u], ub[u], y, table);
+      uint32_t dw[8];
+      if (__all_sync(0xffffffffu, table_words(gb[u], dw))) {
+        swiglu_block_table(dw, ub[u], y, table);
       } else if (__all_sync(0xffffffffu, block_amax(gb[u]) <= kFastLimit)) {
         swiglu_block<true>(gb[u], ub[u], y);
       } else {

@@ -82,18 +82,19 @@ def test_every_bf16_gate(dev):
 
 
 def test_table_window_every_gate_and_its_edges(dev):
-    """Every bf16 gate the per-CTA SiLU table holds (2^-25 <= |g| <= 87, both
-    signs) laid out so that whole warps take the table path, then the same rows
-    with one gate per warp just outside the window (2^-25 minus one bf16 step,
-    87 plus one step), which sends those warps to the direct computation."""
-    mags = np.arange(0x3300, 0x42AF, dtype=np.uint16)
+    """Every bf16 gate the per-CTA SiLU table holds (2^-25 <= |g| <= 127.5, both
+    signs; above 87 its entries come from the general exponential) laid out so
+    that whole warps take the table path, then the same rows with one gate per
+    warp just outside the window (2^-25 minus one bf16 step, 127.5 plus one step),
+    which sends those warps to the direct computation."""
+    mags = np.arange(0x3300, 0x4300, dtype=np.uint16)
     gates = np.concatenate([mags, mags | np.uint16(0x8000)])
     rows, cols = 12, 8192
     gen = np.random.default_rng(7)
     g_bits = gates[gen.permutation(rows * cols) % gates.size].reshape(rows, cols)
     assert set(np.unique(g_bits)) == set(gates.tolist())
     up = workloads.swiglu_inputs(dev, rows=rows, cols=cols, seed=21)[1]
-    for edge in (None, 0x32FF, 0x42AF, 0xC2AF, 0xB2FF):
+    for edge in (None, 0x32FF, 0x4300, 0xC300, 0xB2FF):
         gb = g_bits.copy()
         if edge is not None:
             gb[:, ::512] = edge  # one gate in every 512-column segment
