@@ -40,6 +40,7 @@ namespace {
 
 constexpr int kThreads = 128;   // CTA size of the generic kernel
 constexpr int kLanes128 = 128;  // the lanes of the canonical order
+constexpr int kBlockStages = 5;  // ring stages of the 7,168-column kernel (215 KB of shared memory)
 
 struct AdalnArgs {
   const uint16_t* x;
@@ -538,21 +539,29 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
 // in pass 2, so a thread quantizes whole blocks (one scale computation per
 // block, no exchange between threads) and keeps the tables of only 16 columns
 // (40 registers).  Pass 1 keeps the canonical order: R = NB / 128 = 3 groups of
-// 128 lanes, group g summing row g of each 3-row step (chunk c on lane c % 128).
-// x streams through a ring of kStages steps of R rows, each pass-1 lane copying
-// its own chunks; chunk c sits at slot c ^ ((c >> 3) & 1), which keeps both the
-// pass-1 reads (lane l, chunk l + 128 j) and the pass-2 reads (thread t, chunks
-// 2t and 2t + 1) free of bank conflicts.  A step's rows are read by every thread
-// in pass 2 only after the barrier that follows their pass 1.  The first warp
-// outside the pass-1 groups publishes, per row of the step about to be emitted,
-// the rstd (from the warp totals, one lane per row), the frame and the row's
-// scale offset, and announces them on a named barrier that the other warps wait
-// on before pass 2; the per-row bookkeeping is thus done once per row, not once
-// per thread.  There is no CTA-wide barrier per step: the other warps announce
-// on a second named barrier that a step's totals are posted (which only the
-// stats warp waits on), and a ring stage is refilled only after the "rows
-// published" barrier of the next step, which every warp reaches after its pass 2
-// of the step that stage held.
+// 128 lanes (four warps each), group g summing row g of each 3-row step (chunk c
+// on lane c % 128).  x streams through a ring of kStages steps of R rows, each
+// pass-1 lane copying its own chunks; chunk c sits at slot c ^ ((c >> 3) & 1),
+// which keeps both the pass-1 reads (lane l, chunk l + 128 j) and the pass-2
+// reads (thread t, chunks 2t and 2t + 1) free of bank conflicts.
+// One warp, the stats warp, does no pass 1: per row of the step about to be
+// emitted it publishes the rstd (from the warp totals, one lane per row), the
+// frame and the row's scale offset in shared memory, so the per-row bookkeeping
+// is done once per row, not once per thread.  The warps are not held in step
+// with one another.  Each of the other 13 warps waits on a named barrier of its
+// own (count 64) on which the stats warp arrives once the step's rows are
+// published; a warp that is ahead goes on without waiting for the slowest.
+// After passing its own barrier, each of them arrives on one shared barrier that
+// only the stats warp waits on before it publishes the next step.  That arrival
+// says the warp has posted its pass-1 totals of the next step and finished pass 2
+// of the step before, so neither the published rows nor the totals are
+// overwritten while still to be read, and no warp arrives twice in one phase of
+// any barrier.  A warp past its barrier of step q thus knows that every warp has
+// finished pass 2 of step q - 2, and refills that stage; with five stages a
+// step's copies are issued two steps before its pass 1.  The stats warp is on
+// the critical path of every step (its own pass 2, then the next publication),
+// so it is warp 2: warps go to the SM's four sub-partitions by warp index mod 4,
+// and sub-partition 2 holds three of the 14 warps, not four.
 // Per-row values published by the stats warp for one step.
 struct RowInfo {
   float rstd;
@@ -563,12 +572,14 @@ struct RowInfo {
 template <int NB, int C1, bool AMAX>
 __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   constexpr int R = NB / kLanes128;
-  constexpr int kStages = 4;
+  constexpr int kStages = kBlockStages;
+  constexpr int kAhead = kStages - 2;  // steps in flight ahead of the step being emitted
   constexpr int kChunks = kLanes128 * C1;
   constexpr int64_t kCodeRow = 8 * NB;  // code bytes per row (cols / 2)
   static_assert(kChunks == 2 * NB, "one thread per 16-element block");
-  constexpr int kStatsWarp = R * kLanes128 / 32;
-  static_assert(kStatsWarp < NB / 32, "needs a warp outside the pass-1 groups");
+  constexpr int kStatsWarp = 2;
+  static_assert(NB / 32 == R * 4 + 2 && NB / 32 - 1 <= 13,
+                "one stats warp, one pass-2-only warp, a named barrier (3..15) per warp but the stats warp");
   extern __shared__ uint4 ring[];  // [kStages][R][kChunks]
   __shared__ float inv_table[128];
   __shared__ float totals[2][R][4];
@@ -580,14 +591,16 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   const int t = threadIdx.x;
   const int warp = t >> 5;
   const int lane = t & 31;
-  const int grp = t >> 7;
-  const int l = t & 127;
-  const bool p1 = grp < R;  // warp-uniform
+  const int pi = warp < kStatsWarp ? warp : warp - 1;  // index among the warps but the stats warp
+  const bool p1 = warp != kStatsWarp && pi < R * 4;      // warp-uniform
+  const int grp = pi >> 2;
+  const int l = (pi & 3) * 32 + lane;
   const int64_t quads = a.cols >> 6;
   const float cols_f = static_cast<float>(a.cols);
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
   const int64_t r_end = a.rows * (blockIdx.x + 1) / gridDim.x;
-  const int64_t steps = (r_end - r_begin + R - 1) / R;
+  // steps of this CTA: rows / (blocks * R) + 1 < 2^31 for any x that fits a device
+  const int steps = static_cast<int>((r_end - r_begin + R - 1) / R);
   const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
   // pass-1 lanes: the next row to copy and its ring slot
@@ -595,10 +608,12 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   const int64_t x_step = R * a.ld;
   const int l_slot = l ^ ((l >> 3) & 1);  // chunk c at slot c ^ ((c >> 3) & 1): conflict-free in both passes
   const uint32_t ring_l = ring_base + static_cast<uint32_t>(grp * kChunks + l_slot) * 16;
+  // a step's ring stage is its index mod kStages, kept by a wrapping counter
+  auto stage_after = [](int s, int k) { return s + k >= kStages ? s + k - kStages : s + k; };
   int issued = 0;  // steps issued so far
-  auto issue = [&]() {
-    if (p1 && issued < steps && r_begin + R * issued + grp < r_end) {
-      const uint32_t dst = ring_l + static_cast<uint32_t>((issued % kStages) * R * kChunks) * 16;
+  auto issue = [&](int stage) {  // the next step, into this stage
+    if (p1 && issued < steps && r_begin + R * int64_t{issued} + grp < r_end) {
+      const uint32_t dst = ring_l + static_cast<uint32_t>(stage * R * kChunks) * 16;
 #pragma unroll
       for (int j = 0; j < C1; ++j) cp_async16(dst + j * (kLanes128 * 16), x_next + j * (kLanes128 * 8));
     }
@@ -606,13 +621,13 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
     x_next += x_step;
     ++issued;
   };
-  auto pass1 = [&](int64_t q) {
+  auto pass1 = [&](int q, int stage) {
     if (q >= steps || !p1) return;
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    if (r_begin + R * q + grp < r_end) {
-      const uint4* buf = ring + ((q % kStages) * R + grp) * kChunks + l_slot;
+    if (r_begin + R * int64_t{q} + grp < r_end) {
+      const uint4* buf = ring + (stage * R + grp) * kChunks + l_slot;
 #pragma unroll
       for (int j = 0; j < C1; ++j) accumulate(buf[j * kLanes128], acc);
     }
@@ -620,13 +635,13 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
                           __fadd_rn(__fadd_rn(acc[2].x, acc[2].y), __fadd_rn(acc[3].x, acc[3].y)));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, o));
-    if (lane == 0) totals[q & 1][grp][warp & 3] = tot;
+    if (lane == 0) totals[q & 1][grp][pi & 3] = tot;
   };
   // the stats warp: lane k < R publishes row k of step q
   FrameCursor lane_cursor(a, r_begin + (lane < R ? lane : 0));
-  auto stats = [&](int64_t q) {
+  auto stats = [&](int q) {
     if (q >= steps || lane >= R) return;
-    const int64_t r = r_begin + R * q + lane;
+    const int64_t r = r_begin + R * int64_t{q} + lane;
     const float* T = totals[q & 1][lane];
     RowInfo info;
     info.rstd = rstd_of(__fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3])), cols_f, a.eps);
@@ -646,30 +661,32 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   };
 
 #pragma unroll
-  for (int q = 0; q < kStages - 1; ++q) issue();
-  cp_async_wait<kStages - 2>();  // step 0 landed (this thread's copies)
-  pass1(0);
+  for (int q = 0; q < kAhead; ++q) issue(q);
+  cp_async_wait<kAhead - 1>();  // step 0 landed (this thread's copies)
+  pass1(0, 0);
   __syncthreads();  // inv_table, step 0's totals and copies
 
   uint8_t* code_step = a.codes + r_begin * kCodeRow + t * 8;
   uint8_t* const scale_t = a.scales + (t >> 2) * 512 + (t & 3);
-  for (int64_t q = 0; q < steps; ++q) {
+  int stage = 0;  // of step q
+  for (int q = 0; q < steps; ++q, stage = stage_after(stage, 1)) {
     if (warp == kStatsWarp) {
-      if (q > 0) named_sync(2, NB);  // step q's totals posted; every warp past barrier 1 of step q-1
+      if (q > 0) named_sync(2, NB);  // step q's totals posted; every warp past its barrier of step q-1
       stats(q);
       __syncwarp();
-      named_arrive(1, NB);
+#pragma unroll 1
+      for (int c = 0; c < NB / 32 - 1; ++c) named_arrive(3 + c, 64);  // rows of step q published
       cp_async_commit();  // keep the group count in step with the copying warps
     } else {
-      cp_async_wait<kStages - 3>();  // step q+1 landed (this thread's copies)
-      pass1(q + 1);
-      named_sync(1, NB);  // rows of step q published; every warp done with step q-1
-      if (q + 1 < steps) named_arrive(2, NB);  // step q+1's totals posted
-      issue();  // step q+3 into step q-1's stage
+      cp_async_wait<kAhead - 2>();  // step q+1 landed (this thread's copies)
+      pass1(q + 1, stage_after(stage, 1));
+      named_sync(3 + pi, 64);  // rows of step q published; every warp done with step q-2
+      if (q + 1 < steps) named_arrive(2, NB);  // step q+1's totals posted; done with step q-1
+      issue(stage_after(stage, kAhead));  // step q+3 into step q-2's stage
     }
 
-    const int n = static_cast<int>(r_end - r_begin - R * q < R ? r_end - r_begin - R * q : R);
-    const uint4* buf = ring + (q % kStages) * R * kChunks + 2 * t;
+    const int n = static_cast<int>(r_end - r_begin - R * int64_t{q} < R ? r_end - r_begin - R * int64_t{q} : R);
+    const uint4* buf = ring + stage * R * kChunks + 2 * t;
     const int sw = (t >> 2) & 1;
     RowInfo info[R];
     bool one_frame = n == R;  // all R rows present and in one frame (frames need not be monotone)
@@ -721,7 +738,7 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
 template <bool AMAX>
 cudaError_t launch_block7168(const AdalnArgs& a, cudaStream_t stream) {
   constexpr int NB = 448, C1 = 7, R = NB / kLanes128;
-  const int smem = 4 * R * kLanes128 * C1 * 16;
+  const int smem = kBlockStages * R * kLanes128 * C1 * 16;
   int blocks = 0;
   cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1, AMAX>),
                                       NB, smem, a.rows > 0 ? (a.rows + R - 1) / R : 1, &blocks);
