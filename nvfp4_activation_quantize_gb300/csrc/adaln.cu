@@ -551,17 +551,17 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
 // with one another.  Each of the other 13 warps waits on a named barrier of its
 // own (count 64) on which the stats warp arrives once the step's rows are
 // published; a warp that is ahead goes on without waiting for the slowest.
-// After passing its own barrier, each of them arrives on one shared barrier that
-// only the stats warp waits on before it publishes the next step.  That arrival
-// says the warp has posted its pass-1 totals of the next step and finished pass 2
-// of the step before, so neither the published rows nor the totals are
-// overwritten while still to be read, and no warp arrives twice in one phase of
-// any barrier.  A warp past its barrier of step q thus knows that every warp has
-// finished pass 2 of step q - 2, and refills that stage; with five stages a
-// step's copies are issued two steps before its pass 1.  The stats warp is on
-// the critical path of every step (its own pass 2, then the next publication),
-// so it is warp 2: warps go to the SM's four sub-partitions by warp index mod 4,
-// and sub-partition 2 holds three of the 14 warps, not four.
+// After passing its own barrier of step q, each of them arrives on one shared
+// barrier that only the stats warp waits on before it publishes step q + 1 (and
+// only then emits step q itself, so its own pass 2 is off the others' path).
+// That arrival says the warp has posted its pass-1 totals of step q + 1 and
+// finished pass 2 of step q - 1, so neither the published rows nor the totals
+// are overwritten while still to be read, and no warp arrives twice in one phase
+// of any barrier.  A warp past its barrier of step q thus knows that every warp
+// has finished pass 2 of step q - 2, and refills that stage; with five stages a
+// step's copies are issued two steps before its pass 1.  The stats warp is warp
+// 2: warps go to the SM's four sub-partitions by warp index mod 4, and
+// sub-partition 2 holds three of the 14 warps, not four.
 // Per-row values published by the stats warp for one step.
 struct RowInfo {
   float rstd;
@@ -665,17 +665,25 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   cp_async_wait<kAhead - 1>();  // step 0 landed (this thread's copies)
   pass1(0, 0);
   __syncthreads();  // inv_table, step 0's totals and copies
+  if (warp == kStatsWarp && steps > 0) {
+    stats(0);
+    __syncwarp();
+#pragma unroll 1
+    for (int c = 0; c < NB / 32 - 1; ++c) named_arrive(3 + c, 64);  // rows of step 0 published
+  }
 
   uint8_t* code_step = a.codes + r_begin * kCodeRow + t * 8;
   uint8_t* const scale_t = a.scales + (t >> 2) * 512 + (t & 3);
   int stage = 0;  // of step q
   for (int q = 0; q < steps; ++q, stage = stage_after(stage, 1)) {
     if (warp == kStatsWarp) {
-      if (q > 0) named_sync(2, NB);  // step q's totals posted; every warp past its barrier of step q-1
-      stats(q);
-      __syncwarp();
+      if (q + 1 < steps) {
+        named_sync(2, NB);  // step q+1's totals posted; every warp past its barrier of step q
+        stats(q + 1);
+        __syncwarp();
 #pragma unroll 1
-      for (int c = 0; c < NB / 32 - 1; ++c) named_arrive(3 + c, 64);  // rows of step q published
+        for (int c = 0; c < NB / 32 - 1; ++c) named_arrive(3 + c, 64);  // rows of step q+1 published
+      }
       cp_async_commit();  // keep the group count in step with the copying warps
     } else {
       cp_async_wait<kAhead - 2>();  // step q+1 landed (this thread's copies)

@@ -29,6 +29,7 @@ class Protocol:
     wait_pending = 1     # cp.async groups left pending before pass 1 of step q+1
     issue_after_own_barrier = True
     arrive_after_own_barrier = True
+    stats_ahead = True   # the stats warp publishes step q+1 before its own pass 2 of step q
 
 
 class Race(AssertionError):
@@ -131,8 +132,20 @@ def simulate(steps: int, seed: int, proto=Protocol) -> None:
         wait_group(w, proto.ahead - 1)
         pass1(w, 0)
         yield ("syncthreads",)
+        if w == STATS and proto.stats_ahead and steps > 0:
+            publish(w, 0)
+            for c in range(len(others)):
+                yield ("arrive", 3 + c, 64)
         for q in range(steps):
-            if w == STATS:
+            if w == STATS and proto.stats_ahead:
+                if q + 1 < steps:
+                    yield ("sync", 2, 448)
+                    publish(w, q + 1)
+                    for c in range(len(others)):
+                        yield ("arrive", 3 + c, 64)
+                issued[w] += 1
+                pending[w].append(None)
+            elif w == STATS:
                 if q > 0:
                     yield ("sync", 2, 448)
                 publish(w, q)
@@ -186,10 +199,15 @@ def simulate(steps: int, seed: int, proto=Protocol) -> None:
         raise Race("a barrier phase is left incomplete")
 
 
+class StatsInStep(Protocol):
+    stats_ahead = False  # the stats warp publishes step q, then emits it
+
+
+@pytest.mark.parametrize("proto", [Protocol, StatsInStep])
 @pytest.mark.parametrize("steps", [0, 1, 2, 3, 4, 7])
-def test_protocol_has_no_deadlock_or_race(steps):
-    for seed in range(80):
-        simulate(steps, seed)
+def test_protocol_has_no_deadlock_or_race(steps, proto):
+    for seed in range(60):
+        simulate(steps, seed, proto)
 
 
 class FourStages(Protocol):
