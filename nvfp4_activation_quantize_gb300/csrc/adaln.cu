@@ -544,10 +544,10 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
 // pass-1 lane copying its own chunks; chunk c sits at slot c ^ ((c >> 3) & 1),
 // which keeps both the pass-1 reads (lane l, chunk l + 128 j) and the pass-2
 // reads (thread t, chunks 2t and 2t + 1) free of bank conflicts.
-// One warp, the stats warp, does no pass 1: per row of the step about to be
-// emitted it publishes the rstd (from the warp totals, one lane per row), the
-// frame and the row's scale offset in shared memory, so the per-row bookkeeping
-// is done once per row, not once per thread.  The warps are not held in step
+// One warp, the stats warp, does no pass 1: per row of a step it publishes the
+// rstd (from the warp totals, one lane per row), the frame and the row's scale
+// offset in shared memory, so the per-row bookkeeping is done once per row, not
+// once per thread.  The warps are not held in step
 // with one another.  Each of the other 13 warps waits on a named barrier of its
 // own (count 64) on which the stats warp arrives once the step's rows are
 // published; a warp that is ahead goes on without waiting for the slowest.
@@ -561,7 +561,9 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
 // has finished pass 2 of step q - 2, and refills that stage; with five stages a
 // step's copies are issued two steps before its pass 1.  The stats warp is warp
 // 2: warps go to the SM's four sub-partitions by warp index mod 4, and
-// sub-partition 2 holds three of the 14 warps, not four.
+// sub-partition 2 holds three of the 14 warps, not four.  Pass 1 runs on 12 of
+// the other 13 warps (three rows of four 32-lane groups).
+
 // Per-row values published by the stats warp for one step.
 struct RowInfo {
   float rstd;
@@ -578,7 +580,11 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   constexpr int64_t kCodeRow = 8 * NB;  // code bytes per row (cols / 2)
   static_assert(kChunks == 2 * NB, "one thread per 16-element block");
   constexpr int kStatsWarp = 2;
-  static_assert(NB / 32 == R * 4 + 2 && NB / 32 - 1 <= 13,
+  // The warp with neither pass 1 nor the statistics: on sub-partition 1 for the
+  // quantizing instance; on sub-partition 2, beside the stats warp, for the
+  // abs-max pass, whose lighter pass 2 leaves pass 1 a larger share of the work.
+  constexpr int kPass2Only = AMAX ? 6 : NB / 32 - 1;
+  static_assert(NB / 32 == R * 4 + 2 && NB / 32 - 1 <= 13 && kPass2Only != kStatsWarp,
                 "one stats warp, one pass-2-only warp, a named barrier (3..15) per warp but the stats warp");
   extern __shared__ uint4 ring[];  // [kStages][R][kChunks]
   __shared__ float inv_table[128];
@@ -592,9 +598,11 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   const int warp = t >> 5;
   const int lane = t & 31;
   const int pi = warp < kStatsWarp ? warp : warp - 1;  // index among the warps but the stats warp
-  const bool p1 = warp != kStatsWarp && pi < R * 4;      // warp-uniform
-  const int grp = pi >> 2;
-  const int l = (pi & 3) * 32 + lane;
+  constexpr bool kLastPass2Only = kPass2Only == NB / 32 - 1;
+  const int ppi = kLastPass2Only ? pi : pi - (warp > kPass2Only ? 1 : 0);  // index among the pass-1 warps
+  const bool p1 = warp != kStatsWarp && (kLastPass2Only ? pi < R * 4 : warp != kPass2Only);  // warp-uniform
+  const int grp = ppi >> 2;
+  const int l = (ppi & 3) * 32 + lane;
   const int64_t quads = a.cols >> 6;
   const float cols_f = static_cast<float>(a.cols);
   const int64_t r_begin = a.rows * blockIdx.x / gridDim.x;
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
                           __fadd_rn(__fadd_rn(acc[2].x, acc[2].y), __fadd_rn(acc[3].x, acc[3].y)));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, o));
-    if (lane == 0) totals[q & 1][grp][pi & 3] = tot;
+    if (lane == 0) totals[q & 1][grp][ppi & 3] = tot;
   };
   // the stats warp: lane k < R publishes row k of step q
   FrameCursor lane_cursor(a, r_begin + (lane < R ? lane : 0));

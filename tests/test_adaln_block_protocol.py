@@ -20,7 +20,6 @@ import pytest
 
 NW = 14          # warps of the 448-thread CTA
 STATS = 2        # the stats warp (no pass 1)
-PASS2_ONLY = 13  # the warp with neither pass 1 nor the statistics
 
 
 class Protocol:
@@ -30,6 +29,7 @@ class Protocol:
     issue_after_own_barrier = True
     arrive_after_own_barrier = True
     stats_ahead = True   # the stats warp publishes step q+1 before its own pass 2 of step q
+    pass2_only = 13      # the warp with neither pass 1 nor the statistics (6 in the abs-max pass)
 
 
 class Race(AssertionError):
@@ -38,7 +38,7 @@ class Race(AssertionError):
 
 def simulate(steps: int, seed: int, proto=Protocol) -> None:
     rng = random.Random(seed)
-    p1 = [w for w in range(NW) if w not in (STATS, PASS2_ONLY)]
+    p1 = [w for w in range(NW) if w not in (STATS, proto.pass2_only)]
     others = [w for w in range(NW) if w != STATS]
     clk = [[0] * NW for _ in range(NW)]
 
@@ -203,7 +203,11 @@ class StatsInStep(Protocol):
     stats_ahead = False  # the stats warp publishes step q, then emits it
 
 
-@pytest.mark.parametrize("proto", [Protocol, StatsInStep])
+class AbsMaxPass(Protocol):
+    pass2_only = 6
+
+
+@pytest.mark.parametrize("proto", [Protocol, AbsMaxPass, StatsInStep])
 @pytest.mark.parametrize("steps", [0, 1, 2, 3, 4, 7])
 def test_protocol_has_no_deadlock_or_race(steps, proto):
     for seed in range(60):
