@@ -214,21 +214,21 @@ __device__ __forceinline__ void emit_chunk(const uint4 (&v)[R], const float (&rs
   for (int k = 0; k < R; ++k)
     amax[k] = halves_amax(absmax_bf16x2(absmax_bf16x2(y[k][0], y[k][1]),
                                         absmax_bf16x2(y[k][2], y[k][3])));
-  if (AMAX) {
+  if constexpr (AMAX) {
 #pragma unroll
     for (int k = 0; k < R; ++k)
       if (valid) run_max = fmaxf(run_max, amax[k]);
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int k = 0; k < R; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], 1));
+    for (int k = 0; k < R; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], 1));
 #pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const uint32_t sf = block_scale(amax[k], gsf);
-    const uint32_t codes = codes8(y[k], inv_table[sf]);
-    if (valid) store_word(codes_at[k], codes);
-    // the even thread of the pair writes the block's scale byte
-    if (valid && !(lane & 1)) store_byte(scale_at[k], sf);
+    for (int k = 0; k < R; ++k) {
+      const uint32_t sf = block_scale(amax[k], gsf);
+      const uint32_t codes = codes8(y[k], inv_table[sf]);
+      if (valid) store_word(codes_at[k], codes);
+      // the even thread of the pair writes the block's scale byte
+      if (valid && !(lane & 1)) store_byte(scale_at[k], sf);
+    }
   }
 }
 
@@ -485,7 +485,7 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
                                            uint8_t* const (&codes_at)[R],
                                            uint8_t* const (&scale_at)[R], float gsf,
                                            const float* inv_table, float& run_max) {
-  if (AMAX) {
+  if constexpr (AMAX) {
     // bf16 rounding is monotone in the magnitude, so max |bf16(o)| = bf16(max |o|):
     // the unrounded values' maximum is rounded once per block
 #pragma unroll
@@ -503,34 +503,34 @@ __device__ __forceinline__ void emit_block(const uint32_t (&v)[R][8], const floa
       }
       run_max = fmaxf(run_max, fabsf(bf16_round(am)));
     }
-    return;
-  }
-  float2 y[R][8];
+  } else {
+    float2 y[R][8];
 #pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const float2 rstd2 = make_float2(rstd[k], rstd[k]);
+    for (int k = 0; k < R; ++k) {
+      const float2 rstd2 = make_float2(rstd[k], rstd[k]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const ChunkTables& t = tb[i >> 2];
-      const float2 n = mul2(bf16x2_to_float2(v[k][i]), rstd2);
-      const float2 h = mul2(n, t.gm[i & 3]);
-      const float2 m = mul2(h, t.fc[i & 3]);
-      const float2 o = add_bf16x2_f32(t.sh[i & 3], m);
-      y[k][i] = make_float2(bf16_round(o.x), bf16_round(o.y));
+      for (int i = 0; i < 8; ++i) {
+        const ChunkTables& t = tb[i >> 2];
+        const float2 n = mul2(bf16x2_to_float2(v[k][i]), rstd2);
+        const float2 h = mul2(n, t.gm[i & 3]);
+        const float2 m = mul2(h, t.fc[i & 3]);
+        const float2 o = add_bf16x2_f32(t.sh[i & 3], m);
+        y[k][i] = make_float2(bf16_round(o.x), bf16_round(o.y));
+      }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < R; ++k) {
-    float amax = 0.0f;
+    for (int k = 0; k < R; ++k) {
+      float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(y[k][i].x), fabsf(y[k][i].y)));
-    const uint32_t sf = block_scale(amax, gsf);
-    const float inv = inv_table[sf];
-    const float2 inv2 = make_float2(inv, inv);
-    const uint32_t lo = e2m1x8(mul2(y[k][0], inv2), mul2(y[k][1], inv2), mul2(y[k][2], inv2), mul2(y[k][3], inv2));
-    const uint32_t hi = e2m1x8(mul2(y[k][4], inv2), mul2(y[k][5], inv2), mul2(y[k][6], inv2), mul2(y[k][7], inv2));
-    store_codes(codes_at[k], lo, hi);
-    store_byte(scale_at[k], sf);
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(y[k][i].x), fabsf(y[k][i].y)));
+      const uint32_t sf = block_scale(amax, gsf);
+      const float inv = inv_table[sf];
+      const float2 inv2 = make_float2(inv, inv);
+      const uint32_t lo = e2m1x8(mul2(y[k][0], inv2), mul2(y[k][1], inv2), mul2(y[k][2], inv2), mul2(y[k][3], inv2));
+      const uint32_t hi = e2m1x8(mul2(y[k][4], inv2), mul2(y[k][5], inv2), mul2(y[k][6], inv2), mul2(y[k][7], inv2));
+      store_codes(codes_at[k], lo, hi);
+      store_byte(scale_at[k], sf);
+    }
   }
 }
 
