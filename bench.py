@@ -688,7 +688,30 @@ def measure_producers(h3q, dev, stream, args):
     _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream,
                            flush=lambda: (scrub.fill_(1), clean.sum()))
     res["quantize_8192x7168_l2_flushed_clean"] = entry(quantize_bytes(*x.shape), per, 8192)
-    del x, c, s, scrub, clean
+    del x, c, s
+
+    # The small cases, each launch after the same clean-lines flush. A launch's fixed cost is most of
+    # their time, so they measure latency, not bandwidth.
+    #  - the tiny AdaLN case (64 x 256);
+    #  - the ragged attention-output quantize at 1,000 tokens (18 MB).
+    def flush():
+        scrub.fill_(1)
+        clean.sum()
+
+    w = workloads.tiny_adaln_inputs(dev)
+    g = torch.tensor([calibrate_adaln_gsf(w)], dtype=torch.float32, device=dev)
+    c, s = h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], g, rows_per_frame=w["rows_per_frame"],
+                                       eps=w["eps"], stream=stream)
+    _, per = time_launches(lambda: h3q.h3q_rmsnorm_adaln_nvfp4(
+        w["x"], w["gamma"], w["table"], g, rows_per_frame=w["rows_per_frame"], eps=w["eps"], codes=c,
+        scales=s, stream=stream), n, stream, flush=flush)
+    res["adaln_tiny_64x256_l2_flushed_clean"] = entry(adaln_bytes(64, 256, w["table"].shape[0]), per, 64)
+    x = workloads.attention_output(dev, tokens=1000)
+    g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
+    c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
+    _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream, flush=flush)
+    res["attn_out_quantize_1000x7168_l2_flushed_clean"] = entry(quantize_bytes(*x.shape), per, 1000)
+    del w, x, c, s, scrub, clean
     torch.cuda.empty_cache()
     if not args.no_cpu_baseline:
         for key, kind in (("swiglu_65280x18944", "swiglu"), ("swiglu_packed_bias_65280x18944", "swiglu_packed"),
