@@ -87,6 +87,17 @@ def test_adaln_amax_row_frame_strided(dev):
     _eq(amax, _adaln_amax_oracle(w, rf.numpy()), "adaln amax row_frame")
 
 
+@pytest.mark.parametrize("rows", [1, 2, 3, 4, 5, 7, 458, 1001])
+def test_adaln_amax_7168_ragged_steps(dev, rows):
+    """The 7,168-column block kernel's abs-max instance (its own warp roles) on CTAs of
+    one or a few 3-row steps, the last one short, with a row -> frame array."""
+    cols, frames_n = 7168, 7
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=frames_n, seed=rows + 90)
+    rf = torch.randint(0, frames_n, (rows,), generator=torch.Generator().manual_seed(rows), dtype=torch.int32)
+    amax = h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], row_frame=rf.to(dev), eps=w["eps"])
+    _eq(amax, _adaln_amax_oracle(w, rf.numpy()), f"adaln amax 7168 ragged {rows}")
+
+
 @pytest.mark.parametrize("rows,cols,extreme", [(3, 64, False), (131, 320, True), (257, 18944, False),
                                                (64, 8192, True)])
 def test_swiglu_amax(dev, rows, cols, extreme):
