@@ -100,6 +100,7 @@ def hbm_peak():
 KERNEL_SOURCES = {
     "adaln_block_kernel": ("adaln.cu", "h3q_device.cuh"),
     "swiglu_kernel": ("swiglu.cu", "h3q_device.cuh"),
+    "swiglu_ring_kernel": ("swiglu.cu", "h3q_device.cuh"),
     "quantize_kernel": ("quantize.cu", "h3q_device.cuh"),
 }
 
@@ -523,7 +524,7 @@ def measure_producers(h3q, dev, stream, args):
         h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream)
     _, per = time_launches(lambda: h3q.h3q_swiglu_nvfp4(gate, up, g, c, s, stream=stream), n, stream)
     res["swiglu_65280x18944"] = entry(swiglu_bytes(*gate.shape), per, gate.shape[0])
-    ipe = recorded_value("swiglu_kernel", os.path.join(ROOT, "profiles", "inst_per_element.txt"))
+    ipe = recorded_value("swiglu_ring_kernel", os.path.join(ROOT, "profiles", "inst_per_element.txt"))
     if ipe is not None:
         # the instruction-issue bound: every SM sub-partition issuing one warp
         # instruction per cycle at the clock seen under load

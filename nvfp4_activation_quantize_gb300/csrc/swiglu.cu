@@ -28,7 +28,11 @@
 // the same bits.
 //
 // Work layout as in the standalone quantize: one warp per 512-column segment,
-// one 16-element block per lane, 256-bit loads of gate and up.  In the direct
+// one 16-element block per lane.  The plain producer stages gate and up through
+// a per-warp cp.async ring (swiglu_ring_kernel: one 768-thread CTA per SM, two
+// segments' copies in flight per warp while it computes a third); the abs-max
+// pass and the packed projection with its bias load them with 256-bit loads
+// into registers (swiglu_kernel).  In the direct
 // computation, when every gate of the warp's segment has |g| <= 87, 2^k is a
 // normal number for every element and the scaling is a single multiply by a
 // power of two built from k's bits; otherwise the warp scales with ldexpf,
@@ -41,9 +45,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-// Segments in flight per warp: two for gate and up; one for the packed
-// projection with its bias, whose extra bias loads and adds would otherwise cost
-// the registers of a fourth CTA per SM (52 registers instead of 64).
+// Segments in flight per warp in swiglu_kernel: two for the abs-max pass; one
+// for the packed projection with its bias, whose extra bias loads and adds would
+// otherwise cost the registers of a fourth CTA per SM (52 registers, not 64).
 constexpr int kUnrollPlain = 2;
 
 constexpr float kL2E = 0x1.715476p+0f;    // fl(1 / ln 2)
@@ -297,6 +301,126 @@ swiglu_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t
   if (AMAX) commit_amax(run_max, amax, inv_table);  // inv_table is unused in this mode
 }
 
+// The plain producer with its loads staged through a per-warp cp.async ring:
+// one CTA of 768 threads per SM sharing one SiLU table, each warp one segment
+// per step with the next kRingStages - 1 segments' copies in flight.  Each lane
+// copies and later reads only its own 32 bytes of gate and of up, so only its
+// own cp.async.wait_group orders them; its two 16-byte halves sit swapped in
+// lanes 4-7 of every 8 (slot c ^ ((lane >> 2) & 1)), which keeps the 16-byte
+// shared loads of a quarter-warp on distinct banks.
+constexpr int kRingThreads = 768;
+constexpr int kRingWarps = kRingThreads / 32;
+constexpr int kRingStages = 3;
+constexpr int kRingWarpBytes = kRingStages * 2 * 1024;
+
+__device__ __forceinline__ void ring_cp16(uint32_t smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void ring_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void ring_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ring_ld16(uint32_t smem, uint32_t* w) {
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(smem)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kRingThreads, 1)
+swiglu_ring_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uint16_t* __restrict__ up,
+                   int64_t ld_up, int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
+                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  __shared__ float inv_table[128];
+  __shared__ __align__(16) float silu_table[2 * kTabHalf];
+  extern __shared__ __align__(16) uint8_t ring[];  // [warp][stage][gate, up][lane][32 bytes]
+  const float gsf = *gsf_ptr;
+  fill_inverse_scales(inv_table, gsf);
+  fill_silu_table(silu_table);
+  __syncthreads();
+  const char* table = reinterpret_cast<const char*>(silu_table);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t groups = cols >> 4;
+  const int64_t quads = cols >> 6;
+  const int64_t segs = (groups + 31) >> 5;
+  const int64_t prows = (rows + 127) >> 7 << 7;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRingWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kRingWarps + warp;
+  const int64_t adv_rows = nwarps / segs;
+  const int64_t adv_segs = nwarps - adv_rows * segs;
+  const uint32_t sw = ((lane >> 2) & 1) * 16;
+  const uint32_t mine = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + warp * kRingWarpBytes + lane * 32;
+
+  int64_t crow = first / segs, cseg = first - crow * segs;  // the segment computed
+  int64_t irow = crow, iseg = cseg;                          // the next segment copied
+  auto issue = [&](int stage) {
+    const int64_t g = iseg * 32 + lane;
+    if (irow < rows && g < groups) {
+      const uint32_t d = mine + stage * 2048;
+      const uint16_t* gp = gate + irow * ld_gate + g * kBlock;
+      const uint16_t* upp = up + irow * ld_up + g * kBlock;
+      ring_cp16(d + sw, gp);
+      ring_cp16(d + (sw ^ 16), gp + 8);
+      ring_cp16(d + 1024 + sw, upp);
+      ring_cp16(d + 1024 + (sw ^ 16), upp + 8);
+    }
+    ring_commit();
+    iseg += adv_segs;
+    irow += adv_rows;
+    if (iseg >= segs) {
+      iseg -= segs;
+      irow += 1;
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < kRingStages - 1; ++s) issue(s);
+  int stage = 0;
+  while (crow < prows) {
+    ring_wait<kRingStages - 2>();  // this step's copies (this lane's) landed
+    const int64_t g = cseg * 32 + lane;
+    const bool in_row = crow < rows;
+    const bool in_cols = g < groups;
+    Block16 gb, ub;
+    if (in_row && in_cols) {
+      const uint32_t d = mine + stage * 2048;
+      ring_ld16(d + sw, gb.w);
+      ring_ld16(d + (sw ^ 16), gb.w + 4);
+      ring_ld16(d + 1024 + sw, ub.w);
+      ring_ld16(d + 1024 + (sw ^ 16), ub.w + 4);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gb.w[i] = ub.w[i] = 0;
+    }
+    // the stage read in the previous step (its loads long consumed) takes the
+    // step kRingStages - 1 ahead
+    issue(stage == 0 ? kRingStages - 1 : stage - 1);
+    Block16 y;
+    uint32_t dw[8];
+    if (__all_sync(0xffffffffu, table_words(gb, dw))) {
+      swiglu_block_table(dw, ub, y, table);
+    } else if (__all_sync(0xffffffffu, block_amax(gb) <= kFastLimit)) {
+      swiglu_block<true>(gb, ub, y);
+    } else {
+      swiglu_block<false>(gb, ub, y);
+    }
+    Quantized q = quantize_block<true>(y, gsf, inv_table);
+    if (!in_row) q.sf = 0;
+    if (in_row && in_cols) store_codes(codes + crow * (cols >> 1) + g * 8, q.codes_lo, q.codes_hi);
+    store_scale_quad(scales, crow, g, quads, q.sf, in_cols);
+    stage = stage + 1 == kRingStages ? 0 : stage + 1;
+    cseg += adv_segs;
+    crow += adv_rows;
+    if (cseg >= segs) {
+      cseg -= segs;
+      crow += 1;
+    }
+  }
+  ring_wait<0>();
+}
+
 }  // namespace
 
 cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
@@ -305,12 +429,12 @@ cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t*
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false, false>),
-                                      kThreads, 0, (work + kWarps - 1) / kWarps, &blocks);
+  const int smem = kRingWarps * kRingWarpBytes;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_ring_kernel), kRingThreads, smem,
+                                      (work + kRingWarps - 1) / kRingWarps, &blocks);
   if (err != cudaSuccess) return err;
-  swiglu_kernel<false, false><<<blocks, kThreads, 0, stream>>>(gate, ld_gate, up, ld_up, rows, cols,
-                                                               gsf, codes, scales, nullptr, nullptr,
-                                                               nullptr);
+  swiglu_ring_kernel<<<blocks, kRingThreads, smem, stream>>>(gate, ld_gate, up, ld_up, rows, cols, gsf,
+                                                             codes, scales);
   return cudaGetLastError();
 }
 
