@@ -30,10 +30,14 @@
  *
  * Common conventions
  * ------------------
- * Memory    All pointers are DEVICE pointers into memory owned by the caller.
- *           The library never allocates, frees or keeps a pointer after a call
- *           returns.  Buffers must stay alive until the work queued on
- *           `stream` has finished.
+ * Memory    All pointers are DEVICE pointers into memory owned by the caller
+ *           (the host-buffer call also takes host pointers).  No call allocates
+ *           device or host memory, frees, or keeps a caller's pointer after it
+ *           returns.  Buffers must stay alive until the work queued on `stream`
+ *           has finished.  The one thing the library creates is the pair of
+ *           streams and 11 events of h3q_rmsnorm_adaln_nvfp4_host, once per CUDA
+ *           context on that call's first use in it, kept until the process ends
+ *           (see there).
  * Stream    `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *           default stream).  Every call is asynchronous: it validates its
  *           arguments on the host, launches its kernel on `stream` (the
@@ -60,11 +64,15 @@
  *           (no device, launch failure, or a sticky error from earlier work).
  *           h3q_last_error() returns a message for the calling thread's most
  *           recent failure.  No call aborts, traps or prints.
- * Threads   The calls keep no state between calls except a per-device cache
- *           of launch sizes; they are safe to call from several threads.  The
- *           one exception is h3q_quantize_nvfp4_dynamic, whose abs-max partials
- *           live in a device array inside the library: calls of it that
- *           overlap on one device race (see there).
+ * Threads   The calls keep two kinds of state between calls, both per CUDA
+ *           context (keyed on the context's unique id, so a context destroyed
+ *           and re-created, e.g. by cudaDeviceReset, starts afresh): a cache of
+ *           launch sizes (occupancy, and the raised shared-memory limit of the
+ *           kernels that need one), and the host-buffer call's streams and
+ *           events.  They are safe to call from several threads.  The one
+ *           exception is h3q_quantize_nvfp4_dynamic, whose abs-max partials live
+ *           in a device array inside the library: calls of it that overlap on
+ *           one device race (see there).
  */
 #ifndef H3Q_H
 #define H3Q_H
@@ -290,7 +298,8 @@ int h3q_global_scale_from_amax(const float *amax, float *global_scale, void *str
  * dynamic scale above for the standalone quantize.  On the stream it runs an
  * abs-max pass over x whose CTAs write their partial maxima into a fixed
  * device array inside the library (a file-scope __device__ array of 4,096
- * floats, one per device, its address resolved once per device), reduces them
+ * floats, one per CUDA context, its address looked up in the current context
+ * on every call: a lookup, not an allocation), reduces them
  * into *global_scale = fl(2688 / max |x|) (0 -> 1, +inf clamped), and then
  * quantizes x as h3q_quantize_nvfp4 does with that scale.  Outputs: codes,
  * scales and the global scale used (a device fp32 scalar written here).
@@ -374,7 +383,10 @@ int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, c
  * that device and keeps them; it allocates no memory.  Calls on one device are
  * enqueued one at a time (a lock), and stay asynchronous.  Status codes as the
  * other calls; a failure after the first copy was queued leaves the outputs
- * unspecified.
+ * unspecified.  The streams and events belong to the CUDA context current at the
+ * call (2 streams, 11 events per context, never destroyed: a context that the
+ * caller destroys takes them with it).  At most 64 contexts over the process's
+ * life can use this call; the 65th gets H3Q_ERR_CUDA (cudaErrorNotSupported).
  */
 int h3q_rmsnorm_adaln_nvfp4_host(const void *x_host, int64_t rows, int64_t cols, const void *gamma,
                                  const void *mod_table, int64_t num_frames, const int32_t *row_frame,

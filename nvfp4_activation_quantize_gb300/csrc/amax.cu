@@ -11,7 +11,6 @@
 // global_scale_kernel turns an abs-max into the global scale fl(2688 / amax),
 // with 0 -> 1 and +inf clamped to the largest finite binary32 first.
 #include <cfloat>
-#include <mutex>
 
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
@@ -65,7 +64,7 @@ __global__ void global_scale_kernel(const float* __restrict__ amax, float* __res
 
 // Per-CTA partial maxima of h3q_quantize_nvfp4_dynamic: a file-scope device
 // array, so the call needs no scratch from the caller and allocates nothing.
-// One array per device (per context); calls that overlap on the device share it.
+// One array per context (the module's copy); calls that overlap on the device share it.
 __device__ __align__(256) float g_partial_amax[kMaxDynamicPartials];
 
 // Each CTA writes its own max |x| to partial[blockIdx.x] (no atomics, nothing to
@@ -137,24 +136,14 @@ cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks) {
 
 cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
                                         int blocks, float* gsf, cudaStream_t stream) {
-  // The device address of this context's scratch array, resolved once per device.
-  static std::mutex mutex;
-  static float* address[64] = {};
-  int device = 0;
-  cudaError_t err = cudaGetDevice(&device);
+  // The device address of the scratch array in the current context.  It is
+  // looked up on every call (a lookup, no allocation): a cached address would
+  // point into a context the caller may since have destroyed, or into another
+  // context's copy of the module.
+  void* address = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(&address, g_partial_amax);
   if (err != cudaSuccess) return err;
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  float* partial = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(mutex);
-    if (address[device] == nullptr) {
-      void* p = nullptr;
-      err = cudaGetSymbolAddress(&p, g_partial_amax);
-      if (err != cudaSuccess) return err;
-      address[device] = static_cast<float*>(p);
-    }
-    partial = address[device];
-  }
+  float* partial = static_cast<float*>(address);
   amax_partials_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, partial);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -9,6 +9,8 @@
 #include <mutex>
 #include <string>
 
+#include <cuda.h>  // driver types only; the two driver calls are fetched at run time
+
 #include "../../include/h3q.h"
 #include "h3q_internal.h"
 
@@ -83,34 +85,74 @@ int check_outputs(const char* fn, const uint8_t* codes, const uint8_t* scales,
   return 0;
 }
 
-// --- per-device, per-kernel launch-size cache -------------------------------
+// --- per-context, per-kernel launch-size cache ------------------------------
+
+// A kernel whose attributes a runtime call can query: the query loads the
+// library's module into the current context, which binds the device's primary
+// context to the calling thread when none is current.
+__global__ void context_probe_kernel() {}
 
 struct OccupancyEntry {
   const void* kernel;
-  int device;
+  unsigned long long context;
   int threads;
   int smem_bytes;
   int blocks_per_sm;
   int sms;
 };
+constexpr int kOccEntries = 256;
 std::mutex g_occ_mutex;
-OccupancyEntry g_occ[64];
+OccupancyEntry g_occ[kOccEntries];
 int g_occ_n = 0;
+int g_occ_next = 0;
 
 }  // namespace
 
 namespace h3q {
+
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult found;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &found) ==
+            cudaSuccess && found == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &found) ==
+            cudaSuccess && found == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {  // no context on this thread yet: let the runtime bind the primary one
+    cudaFuncAttributes attr;
+    cudaError_t err = cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(&context_probe_kernel));
+    if (err != cudaSuccess) return err;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
 
 cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, int64_t max_blocks,
                               int* blocks) {
   int device = 0;
   cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return err;
+  // Keyed on the context, not the device ordinal: the shared-memory limit set
+  // below belongs to the context, and a context the caller re-creates (after
+  // cudaDeviceReset, say) starts without it.
+  unsigned long long context = 0;
+  if ((err = current_context_id(&context)) != cudaSuccess) return err;
   int per_sm = 0, sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     for (int i = 0; i < g_occ_n; ++i)
-      if (g_occ[i].kernel == kernel && g_occ[i].device == device && g_occ[i].threads == threads &&
+      if (g_occ[i].kernel == kernel && g_occ[i].context == context && g_occ[i].threads == threads &&
           g_occ[i].smem_bytes == smem_bytes) {
         per_sm = g_occ[i].blocks_per_sm;
         sms = g_occ[i].sms;
@@ -127,7 +169,12 @@ cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, i
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     std::lock_guard<std::mutex> lock(g_occ_mutex);
-    if (g_occ_n < 64) g_occ[g_occ_n++] = {kernel, device, threads, smem_bytes, per_sm, sms};
+    if (g_occ_n < kOccEntries) {
+      g_occ[g_occ_n++] = {kernel, context, threads, smem_bytes, per_sm, sms};
+    } else {  // full (many contexts over the process's life): reuse the slots in turn
+      g_occ[g_occ_next] = {kernel, context, threads, smem_bytes, per_sm, sms};
+      g_occ_next = (g_occ_next + 1) % kOccEntries;
+    }
   }
   int64_t n = static_cast<int64_t>(per_sm) * sms;
   if (max_blocks < n) n = max_blocks;

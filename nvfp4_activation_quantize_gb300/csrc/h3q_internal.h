@@ -6,10 +6,17 @@
 
 namespace h3q {
 
+// The unique id (cuCtxGetId) of the CUDA context current on the calling thread,
+// binding the current device's primary context first when the thread has none.
+// Per-context state of the library (launch-size cache, host-call streams) is
+// keyed on it: ids are never reused within a process, so state left behind by
+// a context the caller destroyed is never taken for the new one's.
+cudaError_t current_context_id(unsigned long long* id);
+
 // Blocks to launch for a persistent kernel: every SM filled to the occupancy
 // the kernel allows at `threads` threads and `smem_bytes` of dynamic shared
 // memory per block, capped at `max_blocks`.  Raises the kernel's dynamic
-// shared memory limit when smem_bytes needs it.  Cached per device, kernel
+// shared memory limit when smem_bytes needs it.  Cached per context, kernel
 // and launch shape.
 cudaError_t persistent_blocks(const void* kernel, int threads, int smem_bytes, int64_t max_blocks,
                               int* blocks);

@@ -19,19 +19,37 @@ namespace h3q {
 namespace {
 
 constexpr int kDepth = 3;  // staging slots: the layout of h3q_host_workspace_bytes
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
-// Internal streams and events of one device, created on its first host call and
-// kept.  The mutex serialises the enqueueing of host calls on the device (they
-// share the streams and events); the calls themselves stay asynchronous.
+// Internal streams and events of one CUDA context, created on its first host
+// call and kept.  The mutex serialises the enqueueing of host calls in the
+// context (they share the streams and events); the calls themselves stay
+// asynchronous.  Keyed on the context's unique id, so a context the caller
+// destroys and re-creates gets fresh streams and events instead of dead handles.
 struct DevicePipe {
   std::mutex mu;
+  unsigned long long context = 0;  // 0: slot unused (context ids start at 1)
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t loaded[kDepth] = {}, computed[kDepth] = {}, drained[kDepth] = {};
 };
-DevicePipe g_pipes[kMaxDevices];
+std::mutex g_pipes_mu;
+DevicePipe g_pipes[kMaxContexts];
+
+// The slot of the current context, claimed on its first call; nullptr once
+// kMaxContexts contexts have claimed one.
+DevicePipe* pipe_of(unsigned long long context) {
+  std::lock_guard<std::mutex> lock(g_pipes_mu);
+  for (DevicePipe& p : g_pipes)
+    if (p.context == context) return &p;
+  for (DevicePipe& p : g_pipes)
+    if (p.context == 0) {
+      p.context = context;
+      return &p;
+    }
+  return nullptr;
+}
 
 cudaError_t init_pipe(DevicePipe& p) {
   cudaError_t err = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking);
@@ -61,11 +79,12 @@ cudaError_t launch_adaln_host(const uint16_t* x_host, int64_t rows, int64_t cols
                               int64_t rows_per_frame, float eps, const float* gsf, uint8_t* codes_host,
                               uint8_t* scales_host, uint8_t* workspace, int64_t chunk_rows,
                               cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  unsigned long long context = 0;
+  cudaError_t err = current_context_id(&context);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  DevicePipe& p = g_pipes[dev];
+  DevicePipe* slot = pipe_of(context);
+  if (slot == nullptr) return cudaErrorNotSupported;  // more contexts than slots
+  DevicePipe& p = *slot;
   std::lock_guard<std::mutex> lock(p.mu);
   if (!p.ready && (err = init_pipe(p)) != cudaSuccess) return err;
 

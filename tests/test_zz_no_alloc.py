@@ -53,6 +53,37 @@ def test_matches_the_existing_entry_points_on_two_calls_in_a_row():
         assert torch.equal(scales, ref_scales), f"scales differ for {rows} x {cols}"
 
 
+@pytest.mark.gpu
+def test_a_call_leaves_device_memory_as_it_found_it():
+    """After a first call on the device, further calls change no free-memory count:
+    the partial maxima go to the library's own array, and nothing is allocated."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    x = workloads.attention_output(dev, tokens=2048, seed=43)
+    rows, cols = x.shape
+    gsf = torch.empty(1, dtype=torch.float32, device=dev)
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((h3q.padded_rows(rows), cols // 16), dtype=torch.uint8, device=dev)
+    lib = h3q.library()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call():
+        rc = lib.h3q_quantize_nvfp4_dynamic(x.data_ptr(), cols, rows, cols, gsf.data_ptr(),
+                                            codes.data_ptr(), scales.data_ptr(), stream)
+        assert rc == h3q.H3Q_OK, h3q.h3q_last_error()
+
+    call()
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info(dev)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info(dev)
+    assert free_after == free_before, f"free device memory moved by {free_before - free_after} bytes"
+
+
 def test_host_checks_run_before_any_cuda_call():
     libbuild.build()
     lib = h3q.library()
