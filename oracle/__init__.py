@@ -69,6 +69,9 @@ _SIGNATURES = {
     "orc_global_scale": ([_F], _F),
     "orc_amax_bf16": ([_P, _I64], _F),
     "orc_row_rstd_f32": ([_P, _I64, _F], _F),
+    "orc_sumsq_bf16": ([_P, _I64, ctypes.c_int], _F),
+    "orc_sumsq_f32": ([_P, _I64, ctypes.c_int], _F),
+    "orc_head_rstd": ([_P, _I64, _F], _F),
     "orc_qkv_epilogue_rows": ([_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _I64, ctypes.c_int, _F,
                                _P], None),
     "orc_swiglu_packed_rows": ([_P, _I64, _P, _I64, _I64, _F, _P, _P, _P, _P], None),
@@ -270,6 +273,36 @@ def quantize_rows(x_bits: np.ndarray, gsf: float, threads: int = 1):
     return codes, sf
 
 
+def sumsq_bf16(bits: np.ndarray, lanes: int = 128) -> float:
+    """The canonical sum of squares of bf16 values (bit patterns): 128 lanes for a
+    row, hd/8 for a head of hd values."""
+    x = _u16(bits).ravel()
+    _check_lanes(x.size, lanes)
+    return float(lib().orc_sumsq_bf16(_ptr(x), x.size, int(lanes)))
+
+
+def sumsq_f32(values: np.ndarray, lanes: int = 128) -> float:
+    """The canonical sum of squares of binary32 values (same order as sumsq_bf16)."""
+    v = np.ascontiguousarray(values, dtype=np.float32).ravel()
+    _check_lanes(v.size, lanes)
+    return float(lib().orc_sumsq_f32(_ptr(v), v.size, int(lanes)))
+
+
+def _check_lanes(n: int, lanes: int) -> None:
+    if n % 8 or not (lanes == 128 or lanes in (2, 4, 8, 16, 32)):
+        raise ValueError(f"the canonical order takes n % 8 == 0 and 128 or 2..32 (a power of two) "
+                         f"lanes, got n={n}, lanes={lanes}")
+    if lanes != 128 and n != 8 * lanes:
+        raise ValueError("a head has one chunk per lane: n must be 8 * lanes")
+
+
+def head_rstd(values: np.ndarray, eps: float) -> float:
+    """rstd of one head of the QKV epilogue: hd binary32 values, hd/8 lanes."""
+    v = np.ascontiguousarray(values, dtype=np.float32).ravel()
+    _check_lanes(v.size, v.size // 8)
+    return float(lib().orc_head_rstd(_ptr(v), v.size, float(eps)))
+
+
 def row_rstd(x_row_bits: np.ndarray, eps: float) -> float:
     x = _u16(x_row_bits)
     _check_cols(x.size)
@@ -421,7 +454,8 @@ def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: fl
     x = _u16(x_bits)
     n, d = x.shape
     hd = d // heads
-    assert hd * heads == d and hd % 16 == 0 and hd <= 1024
+    # the canonical order takes hd/8 lanes, a power of two up to 32
+    assert hd * heads == d and hd in (16, 32, 64, 128, 256)
     bias = _u16(bias_bits).reshape(d)
     # ROT is the tables' width; no tables is ROT = 0: the norm without a rotation
     cos = _u16(cos_bits) if cos_bits is not None else np.zeros((n, 0), np.uint16)

@@ -371,47 +371,80 @@ void orc_quantize_rows(const uint16_t *x, int64_t nrows, int64_t cols, int64_t l
 }
 
 /*
- * RMS statistics of one row in the canonical order.  The row's 8-element
- * chunks (chunk c = columns 8c..8c+7) are dealt round-robin to 128 lanes
- * (chunk c to lane c % 128).  Each lane keeps eight fp32 partials; element e
- * of each of its chunks, chunks in increasing order, goes into partial e
- * through a fused multiply-add ("sequential FMA per thread", [FV-API]
- * introduction).  A lane's total is ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).  The
- * lanes form four groups of 32 (lanes 32w..32w+31); inside a group a
- * butterfly -- for o = 16, 8, 4, 2, 1 every lane adds the total of lane
- * (l xor o) -- leaves each lane holding the group total T_w, and
- *   ss   = (T_0 + T_1) + (T_2 + T_3)
- *   mean = fl(ss / cols),  rstd = fl(1 / fl(sqrt(fl(mean + eps)))).
+ * Sum of squares in the canonical order.  This is the one routine behind every
+ * RMS statistic of the oracle (bf16 rows, fp32 rows of the residual fold, and
+ * the heads of the QKV epilogue); the order is a definition of this build,
+ * fixed here and pinned bit for bit by hand-derived rows, and kernels follow it.
+ *
+ * The n values (n a multiple of 8) form 8-element chunks, chunk c = values
+ * 8c..8c+7.  Chunks are dealt round-robin to `lanes` lanes (chunk c to lane
+ * c % lanes).  Each lane keeps eight fp32 partials starting at +0; element e of
+ * each of its chunks, chunks in increasing order, goes into partial e through a
+ * fused multiply-add ("sequential FMA per thread", [FV-API] introduction).  A
+ * lane's total is ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).  The lanes form groups
+ * of G = min(lanes, 32) consecutive lanes; inside a group a butterfly -- for
+ * o = G/2, ..., 2, 1 every lane adds the total of lane (l xor o) -- leaves each
+ * lane holding the group total.  One group: that total is the sum.  Four groups
+ * (lanes = 128, the rows): ss = (T_0 + T_1) + (T_2 + T_3).
+ * `lanes` is 128 for rows and hd/8 (a power of two up to 32) for heads.
+ * Values come from `b16` (bf16 bit patterns, exact in binary32) when it is not
+ * NULL, else from `f32`.
  */
-float orc_row_rstd(const uint16_t *xrow, int64_t cols, float eps)
+static float canonical_sumsq(const uint16_t *b16, const float *f32, int64_t n, int lanes)
 {
-    int64_t chunks = cols / 8;
+    int64_t chunks = n / 8;
     float lane[128];
-    for (int l = 0; l < 128; ++l) {
+    for (int l = 0; l < lanes; ++l) {
         float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        for (int64_t c = l; c < chunks; c += 128)
+        for (int64_t c = l; c < chunks; c += lanes)
             for (int e = 0; e < 8; ++e) {
-                float v = orc_bf16_value(xrow[8 * c + e]);
+                float v = b16 ? orc_bf16_value(b16[8 * c + e]) : f32[8 * c + e];
                 p[e] = fmaf(v, v, p[e]);
             }
         lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
     }
-    float group[4];
-    for (int w = 0; w < 4; ++w) {
+    int width = lanes < 32 ? lanes : 32;
+    float total[4];
+    for (int w = 0; w < lanes / width; ++w) {
         float g[32];
-        memcpy(g, lane + 32 * w, sizeof g);
-        for (int o = 16; o >= 1; o /= 2) {
+        memcpy(g, lane + width * w, sizeof(float) * (size_t)width);
+        for (int o = width / 2; o >= 1; o /= 2) {
             float next[32];
-            for (int l = 0; l < 32; ++l)
+            for (int l = 0; l < width; ++l)
                 next[l] = g[l] + g[l ^ o];
-            memcpy(g, next, sizeof g);
+            memcpy(g, next, sizeof(float) * (size_t)width);
         }
-        group[w] = g[0];
+        total[w] = g[0];
     }
-    float ss = (group[0] + group[1]) + (group[2] + group[3]);
-    float mean = ss / (float)cols;
+    if (lanes / width == 1)
+        return total[0];
+    return (total[0] + total[1]) + (total[2] + total[3]);
+}
+
+/* rstd = fl(1 / fl(sqrt(fl(fl(ss / n) + eps)))): correctly rounded division and
+ * square root, eps added after the mean. */
+static float rstd_of_sumsq(float ss, int64_t n, float eps)
+{
+    float mean = ss / (float)n;
     float root = sqrtf(mean + eps);
     return 1.0f / root;
+}
+
+/* The canonical sum of squares of n values (bf16 bits or binary32) with the given
+ * number of lanes (128 for a row; hd/8 for a head of hd values). */
+float orc_sumsq_bf16(const uint16_t *v, int64_t n, int lanes) { return canonical_sumsq(v, NULL, n, lanes); }
+float orc_sumsq_f32(const float *v, int64_t n, int lanes) { return canonical_sumsq(NULL, v, n, lanes); }
+
+/* rstd of one bf16 row (128 lanes). */
+float orc_row_rstd(const uint16_t *xrow, int64_t cols, float eps)
+{
+    return rstd_of_sumsq(canonical_sumsq(xrow, NULL, cols, 128), cols, eps);
+}
+
+/* rstd of one fp32 row (128 lanes): the residual fold's statistics. */
+float orc_row_rstd_f32(const float *row, int64_t cols, float eps)
+{
+    return rstd_of_sumsq(canonical_sumsq(NULL, row, cols, 128), cols, eps);
 }
 
 /*
@@ -509,24 +542,11 @@ void orc_swiglu_packed_rows(const uint16_t *o, int64_t ld_o, const uint16_t *bia
  *   commit "...fused RMSNorm+RoPE kernels": interleaved RoPE on the native
  *   [B, S, H, D] layout): r_{2j} = -n_{2j+1}, r_{2j+1} = n_{2j}, same out_i.
  */
-static float head_rstd(const float *v, int64_t hd, float eps)
+/* rstd of one head of hd values (hd a power of two, 16..256): the canonical
+ * order with hd/8 lanes, one chunk per lane. */
+float orc_head_rstd(const float *v, int64_t hd, float eps)
 {
-    int64_t lanes = hd / 8;
-    float lane[128];
-    for (int64_t l = 0; l < lanes; ++l) {
-        float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        for (int e = 0; e < 8; ++e)
-            p[e] = fmaf(v[8 * l + e], v[8 * l + e], p[e]);
-        lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-    }
-    for (int64_t o = lanes / 2; o >= 1; o /= 2) {
-        float next[128];
-        for (int64_t l = 0; l < lanes; ++l)
-            next[l] = lane[l] + lane[l ^ o];
-        memcpy(lane, next, sizeof(float) * (size_t)lanes);
-    }
-    float mean = lane[0] / (float)hd;
-    return 1.0f / sqrtf(mean + eps);
+    return rstd_of_sumsq(canonical_sumsq(NULL, v, hd, (int)(hd / 8)), hd, eps);
 }
 
 void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias, int64_t nrows,
@@ -547,7 +567,7 @@ void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias
                     oh[i] = orc_bf16_bits(xb[i]);
                 continue;
             }
-            float rstd = head_rstd(xb, hd, eps);
+            float rstd = orc_head_rstd(xb, hd, eps);
             for (int64_t i = 0; i < hd; ++i)
                 n[i] = orc_bf16_round(xb[i] * rstd);
             for (int64_t i = 0; i < hd; ++i) {
@@ -584,37 +604,6 @@ void orc_qkv_epilogue_rows(const uint16_t *x, int64_t ld_x, const uint16_t *bias
  * and then the RMSNorm + AdaLN spec above on the fp32 values h' (the same
  * canonical reduction order, squares by fmaf of fp32 values).
  */
-float orc_row_rstd_f32(const float *row, int64_t cols, float eps)
-{
-    int64_t chunks = cols / 8;
-    float lane[128];
-    for (int l = 0; l < 128; ++l) {
-        float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        for (int64_t c = l; c < chunks; c += 128)
-            for (int e = 0; e < 8; ++e) {
-                float v = row[8 * c + e];
-                p[e] = fmaf(v, v, p[e]);
-            }
-        lane[l] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-    }
-    float group[4];
-    for (int w = 0; w < 4; ++w) {
-        float g[32];
-        memcpy(g, lane + 32 * w, sizeof g);
-        for (int o = 16; o >= 1; o /= 2) {
-            float next[32];
-            for (int l = 0; l < 32; ++l)
-                next[l] = g[l] + g[l ^ o];
-            memcpy(g, next, sizeof g);
-        }
-        group[w] = g[0];
-    }
-    float ss = (group[0] + group[1]) + (group[2] + group[3]);
-    float mean = ss / (float)cols;
-    float root = sqrtf(mean + eps);
-    return 1.0f / root;
-}
-
 void orc_residual_adaln_rows(float *h, int64_t nrows, int64_t cols, int64_t ld_h,
                              const uint16_t *o, int64_t ld_o, const uint16_t *bias,
                              const uint16_t *gate, const uint16_t *gamma, const uint16_t *table,
