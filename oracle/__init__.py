@@ -15,6 +15,8 @@ Functions here mirror the four library calls on host arrays:
 * :func:`adaln_rows`     -- RMSNorm (fp32 statistics) + AdaLN modulation -> NVFP4
 * :func:`swiglu_rows`    -- silu(gate) * up -> NVFP4
 * :func:`dequantize_rows`-- codes + block scales -> fp32
+* :func:`nvfp4_gemm`, :func:`swiglu_epilogue_rows` -- the block-scaled NVFP4 GEMM
+  (exact sum, rounded once) and its SwiGLU + NVFP4 epilogue
 
 plus :func:`swizzle_scales` (logical [rows, cols/16] scales to the 128x4
 layout with zeroed padding rows) and the element-wise conversions the pin
@@ -72,6 +74,8 @@ _SIGNATURES = {
     "orc_sumsq_bf16": ([_P, _I64, ctypes.c_int], _F),
     "orc_sumsq_f32": ([_P, _I64, ctypes.c_int], _F),
     "orc_head_rstd": ([_P, _I64, _F], _F),
+    "orc_nvfp4_gemm_rows": ([_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P], None),
+    "orc_swiglu_epilogue_rows": ([_P, _I64, _I64, _F, _F, _P, _P, _P, _P], None),
     "orc_qkv_epilogue_rows": ([_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, _I64, ctypes.c_int, _F,
                                _P], None),
     "orc_swiglu_packed_rows": ([_P, _I64, _P, _I64, _I64, _F, _P, _P, _P, _P], None),
@@ -472,6 +476,61 @@ def qkv_epilogue_rows(x_bits, bias_bits, heads: int, cos_bits, sin_bits, eps: fl
 
     _run(work, n, threads)
     return out
+
+
+def nvfp4_gemm(a_codes: np.ndarray, a_sf: np.ndarray, b_codes: np.ndarray, b_sf: np.ndarray,
+               threads: int = 1) -> np.ndarray:
+    """acc [m, n] = fl(exact sum over k of a * b) of NVFP4 A [m, k] (codes [m, k/2],
+    logical scales [m, k/16]) and B [n, k] (codes [n, k/2], scales [n, k/16])."""
+    a = np.ascontiguousarray(a_codes, dtype=np.uint8)
+    b = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    sfa = np.ascontiguousarray(a_sf, dtype=np.uint8)
+    sfb = np.ascontiguousarray(b_sf, dtype=np.uint8)
+    m, half = a.shape
+    n = b.shape[0]
+    k = 2 * half
+    if k % 16 or k > 2**19:
+        raise ValueError("k must be a multiple of 16, at most 2^19")
+    assert b.shape == (n, half) and sfa.shape == (m, k // 16) and sfb.shape == (n, k // 16)
+    if any(((sf & 0x80) != 0).any() or (sf == 0x7F).any() for sf in (sfa, sfb)):
+        raise ValueError("scale bytes must be E4M3 codes 0x00..0x7E")
+    acc = np.empty((m, n), np.float32)
+
+    def work(span):
+        i0, i1 = span
+        au = np.empty(k, np.int64)
+        bu = np.empty(k, np.int64)
+        lib().orc_nvfp4_gemm_rows(_ptr(a), _ptr(sfa), i0, i1, k, _ptr(b), _ptr(sfb), n, _ptr(au),
+                                  _ptr(bu), _ptr(acc[i0:i1]))
+
+    _run(work, m, threads)
+    return acc
+
+
+def swiglu_epilogue_rows(acc: np.ndarray, alpha: float, gsf: float | None, want_y: bool = False,
+                         threads: int = 1):
+    """The GEMM's SwiGLU + NVFP4 epilogue on acc [m, n] (column 2j the value, 2j+1
+    the gate of output j): returns (codes [m, n/4], logical scales [m, n/32], y bf16
+    bits [m, n/2] or None)."""
+    acc = np.ascontiguousarray(acc, dtype=np.float32)
+    m, n = acc.shape
+    f = n // 2
+    _check_cols(f)
+    quant = gsf is not None
+    codes = np.empty((m, f // 2), np.uint8) if quant else None
+    sf = np.empty((m, f // 16), np.uint8) if quant else None
+    y = np.empty((m, f), np.uint16) if want_y else None
+
+    def work(span):
+        a, b = span
+        scratch = np.empty(f, np.float32)
+        lib().orc_swiglu_epilogue_rows(_ptr(acc[a:b]), b - a, n, float(alpha),
+                                       float(gsf if quant else 1.0), _ptr(scratch),
+                                       _ptr(codes[a:b]) if quant else None,
+                                       _ptr(sf[a:b]) if quant else None, _ptr(y[a:b]) if want_y else None)
+
+    _run(work, m, threads)
+    return codes, sf, y
 
 
 def dequantize_rows(codes: np.ndarray, sf_logical: np.ndarray, gsf: float,

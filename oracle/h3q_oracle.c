@@ -27,6 +27,10 @@
  *             SiLU-and-mul producer, attention-output quantize).
  *   [FV-LOG]  FastVideo commit log, branch vae-parallel-decode: the modulation
  *             index contract [0, table_rows) and the int64 indexing fix.
+ *   [FV-CUH]  also minimax_h3_swiglu_gemm.cu on the same compare page
+ *             (launch_gemm_swiglu, h3_epilogue::Store): the block-scaled NVFP4
+ *             GEMM with value/gate-paired columns and the SwiGLU + NVFP4
+ *             epilogue.
  *   [FV-API], NVFP4DecoderLinear; [FlashRT] FlashRT PR #142 "FP8/NVFP4
  *             kernelized inference pipeline", commit "...amax pipeline": the
  *             dynamic (per-call abs-max) and calibrated (running-max) scales.
@@ -656,6 +660,97 @@ void orc_swiglu_rows(const uint16_t *gate, int64_t ld_gate, const uint16_t *up, 
         if (codes)
             quantize_row_values(scratch_row, cols, gsf, codes + r * (cols / 2),
                                 sf + r * (cols / 16));
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block-scaled NVFP4 GEMM, then the SwiGLU + NVFP4 epilogue                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * [FV-CMP] minimax_h3_swiglu_gemm.cu (launch_gemm_swiglu, h3_epilogue::Store):
+ * the FFN-up projection as a block-scaled NVFP4 GEMM whose epilogue applies the
+ * SwiGLU on value/gate-paired columns and writes NVFP4 directly.  A is the
+ * activation [m, k] and B the weight [n, k], both NVFP4 (E2M1 codes, one E4M3
+ * scale per 16 elements along k); n = 2F, and output j pairs column 2j (the
+ * value) with column 2j + 1 (the gate).
+ *
+ * The GEMM: acc[i][j] = fl(sum over k of a_ik * b_jk) with a_ik =
+ * E2M1value(code) * E4M3value(scale), each product and the whole sum taken
+ * exactly and rounded once to binary32.  (Every element is an integer times
+ * 2^-10, every product an integer times 2^-20, so the sum is an exact integer
+ * in int64 for k <= 2^19; converting it to binary32 is one correctly rounded
+ * conversion, and the scaling by 2^-20 is exact.)  A tensor core adds its
+ * partial products in its own order; this exact sum is what it approximates.
+ *
+ * The epilogue (reading of h3_epilogue::Store with the SwiGLU and the block
+ * quantize of this library):
+ *   u = bf16(fl(alpha * acc[2j])),  g = bf16(fl(alpha * acc[2j + 1]))
+ *   y = bf16(fl(fl(g * sigma(g)) * u)),  sigma(g) = fl(1 / fl(1 + exp_c(-g)))
+ * and y [m, F] is block-quantized with the global scale gsf.
+ */
+
+/* E2M1value(code) * E4M3value(sf) as an integer times 2^-10.  The E4M3 value
+ * is mant * 2^(e - 10) for a normal code (mant = 8 + m) and m * 2^-9 for a
+ * subnormal one; the E2M1 magnitude is i / 2 with i in {0,1,2,3,4,6,8,12}. */
+static int64_t nvfp4_units(uint8_t code, uint8_t sf)
+{
+    static const int twice_e2m1[8] = {0, 1, 2, 3, 4, 6, 8, 12};
+    int e = (sf >> 3) & 15;
+    int m = sf & 7;
+    int64_t mant = e == 0 ? m : 8 + m;
+    int shift = e == 0 ? 0 : e - 1; /* value * 2^10 = i * mant * 2^shift */
+    int64_t v = ((int64_t)twice_e2m1[code & 7] * mant) << shift;
+    return (code & 8) ? -v : v;
+}
+
+/* One operand row as integers (units of 2^-10): codes [k/2] (even element in
+ * the low nibble) and logical scales [k/16]. */
+static void nvfp4_row_units(const uint8_t *codes, const uint8_t *sf, int64_t k, int64_t *out)
+{
+    for (int64_t e = 0; e < k; ++e) {
+        uint8_t byte = codes[e / 2];
+        uint8_t c = (e % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+        out[e] = nvfp4_units(c, sf[e / 16]);
+    }
+}
+
+/* acc [m, n] (rows i0..i1 of it) of A codes [m, k/2] with logical scales
+ * [m, k/16] and B codes [n, k/2] with logical scales [n, k/16].  a_units and
+ * b_units are scratch of k int64 each (per row of A, of B). */
+void orc_nvfp4_gemm_rows(const uint8_t *a, const uint8_t *sfa, int64_t i0, int64_t i1, int64_t k,
+                         const uint8_t *b, const uint8_t *sfb, int64_t n, int64_t *a_units,
+                         int64_t *b_units, float *acc)
+{
+    /* B rows outermost: each converted once, then dotted with the block's A rows */
+    for (int64_t j = 0; j < n; ++j) {
+        nvfp4_row_units(b + j * (k / 2), sfb + j * (k / 16), k, b_units);
+        for (int64_t i = i0; i < i1; ++i) {
+            nvfp4_row_units(a + i * (k / 2), sfa + i * (k / 16), k, a_units);
+            int64_t sum = 0;
+            for (int64_t e = 0; e < k; ++e)
+                sum += a_units[e] * b_units[e];
+            acc[(i - i0) * n + j] = ldexpf((float)sum, -20);
+        }
+    }
+}
+
+/* The SwiGLU + NVFP4 epilogue of nrows rows of acc [nrows, n]: y [nrows, n/2],
+ * quantized into codes [nrows, n/4] and logical scales [nrows, n/32]. */
+void orc_swiglu_epilogue_rows(const float *acc, int64_t nrows, int64_t n, float alpha, float gsf,
+                              float *scratch_row, uint8_t *codes, uint8_t *sf, uint16_t *y_out)
+{
+    int64_t f = n / 2;
+    for (int64_t r = 0; r < nrows; ++r) {
+        for (int64_t j = 0; j < f; ++j) {
+            float u = orc_bf16_round(alpha * acc[r * n + 2 * j]);
+            float g = orc_bf16_round(alpha * acc[r * n + 2 * j + 1]);
+            float y = orc_swiglu_value(g, u);
+            scratch_row[j] = y;
+            if (y_out)
+                y_out[r * f + j] = orc_bf16_bits(y);
+        }
+        if (codes)
+            quantize_row_values(scratch_row, f, gsf, codes + r * (f / 2), sf + r * (f / 16));
     }
 }
 

@@ -48,3 +48,28 @@ def test_every_row(dev, tokens):
     co, so = oracle.quantize_rows(bits(x), gsf, threads=THREADS)
     check_full(codes, scales, tokens, 7168, co, so, f"attention output S={tokens}")
     check_padding(scales, tokens, 7168, f"attention output S={tokens}")
+
+
+def test_dequantize_past_2_31_elements(dev):
+    """The dequantize on the S = 300,000 attention output (2,150,400,000 elements, so
+    output offsets past 2^31): rows 0-255, the last 256 and 4,096 random rows of its
+    fp32 output, bit for bit against the oracle's dequantize of the oracle's codes and
+    scales of the same rows."""
+    tokens, cols = 300000, 7168
+    x = workloads.attention_output(dev, tokens=tokens)
+    assert x.numel() > 2**31
+    gsf = oracle.global_scale(float(x.abs().max().float()))
+    g = gsf_tensor(gsf, dev)
+    codes, scales = h3q.h3q_quantize_nvfp4(x, g)
+    out = h3q.h3q_dequantize_nvfp4(codes, scales, g)
+    del codes, scales
+    rng = np.random.default_rng(2031)
+    sample = np.unique(np.concatenate([np.arange(256), np.arange(tokens - 256, tokens),
+                                       rng.integers(256, tokens - 256, 4096)]))
+    assert sample.max() * cols > 2**31
+    idx = torch.as_tensor(sample, device=dev)
+    got = out.index_select(0, idx).cpu().numpy()
+    co, so = oracle.quantize_rows(bits(x.index_select(0, idx)), gsf, threads=THREADS)
+    want = oracle.dequantize_rows(co, so, gsf, threads=THREADS)
+    bad = np.nonzero((got.view(np.uint32) != want.view(np.uint32)).any(1))[0]
+    assert bad.size == 0, f"dequantize differs in rows {sample[bad[:8]].tolist()}"
