@@ -96,6 +96,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# NVFP4 dense tensor rate over bf16 dense (nominal 13.5 / 2.25 PFLOP/s per GB300).
+FP4_OVER_BF16 = 6.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def fp4_peak():
+    """The NVFP4 dense tensor peak in TFLOP/s: the measured cuBLAS bf16 burst rate
+    times the nominal FP4:bf16 ratio (no FP4 rate is measured on the pool)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]) * FP4_OVER_BF16, "measured bf16 burst x 6 (13.5/2.25 nominal)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, "fallback bf16 x 6"
+
+
 # The sources each kernel is compiled from (its own file and the shared device header).
 KERNEL_SOURCES = {
     "adaln_block_kernel": ("adaln.cu", "h3q_device.cuh"),
@@ -286,6 +302,29 @@ def calibrate_swiglu_gsf(gate, up) -> float:
         y = torch.nn.functional.silu(g) * up[r0:r0 + 4096].float()
         amax = max(amax, float(y.abs().max()))
     return 2688.0 / amax
+
+
+def gemm_operands(h3q, dev, stream, rows: int, hidden: int = COLS, ffn: int = workloads.FFN, seed: int = 8):
+    """The FFN-up GEMM's NVFP4 operands (the activation and the value/gate-paired
+    weight quantized by the library's own quantize), alpha, and the output's global
+    scale from a calibration launch's y (torch abs-max), all outside any timed
+    region.  Returns (operands tuple for h3q_gemm_swiglu_nvfp4, flops per launch)."""
+    w = workloads.ffn_up_inputs(dev, rows=rows, hidden=hidden, ffn=ffn, seed=seed)
+    ops = []
+    gs = []
+    for t in (w["x"], w["w"]):
+        g = 2688.0 / float(t.abs().max().float())
+        c, sc = h3q.h3q_quantize_nvfp4(t, torch.tensor([g], dtype=torch.float32, device=dev), stream=stream)
+        ops += [c, sc]
+        gs.append(g)
+    del w
+    alpha = torch.tensor([1.0 / (gs[0] * gs[1])], dtype=torch.float32, device=dev)
+    y = torch.empty((rows, ffn), dtype=torch.bfloat16, device=dev)
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    h3q.h3q_gemm_swiglu_nvfp4(ops[0], ops[1], ops[2], ops[3], alpha, one, y=y, stream=stream)
+    gsf = torch.tensor([2688.0 / float(y.abs().max().float())], dtype=torch.float32, device=dev)
+    del y
+    return (ops[0], ops[1], ops[2], ops[3], alpha, gsf), 2 * rows * 2 * ffn * hidden
 
 
 # --------------------------------------------------------------------------- #
@@ -691,6 +730,26 @@ def measure_producers(h3q, dev, stream, args):
     res["quantize_8192x7168_l2_flushed_clean"] = entry(quantize_bytes(*x.shape), per, 8192)
     del x, c, s
 
+    # The FFN-up projection as a block-scaled NVFP4 GEMM with the SwiGLU + NVFP4
+    # epilogue (65,280 x 7,168 -> 2 x 18,944): tensor-bound, so TFLOP/s against the
+    # NVFP4 dense peak.
+    torch.cuda.empty_cache()
+    ops, flops = gemm_operands(h3q, dev, stream, ROWS)
+    c, s = h3q.h3q_gemm_swiglu_nvfp4(*ops, stream=stream)
+    for _ in range(3):
+        h3q.h3q_gemm_swiglu_nvfp4(*ops, c, s, stream=stream)
+    _, per = time_launches(lambda: h3q.h3q_gemm_swiglu_nvfp4(*ops, c, s, stream=stream), min(n, 20), stream)
+    ms = sorted(per)[len(per) // 2]
+    tpeak, tsrc = fp4_peak()
+    tflops = flops / (ms * 1e-3) / 1e12
+    res["gemm_swiglu_nvfp4_65280x7168x37888"] = {
+        "bound": "tensor", "tflops": round(tflops, 1), "peak_tflops": round(tpeak, 1), "peak_source": tsrc,
+        "frac_of_peak": round(tflops / tpeak, 4), "frac_of_nominal_13_5_pf": round(tflops / 13500.0, 4),
+        "median_launch_ms": round(ms, 4), "flops": flops, "rows_per_s": round(ROWS / (ms * 1e-3)),
+        "launches": len(per), "error_flag": h3q.h3q_gemm_error_flag()}
+    del ops, c, s
+    torch.cuda.empty_cache()
+
     # The small cases, each launch after the same clean-lines flush. A launch's fixed cost is most of
     # their time, so they measure latency, not bandwidth.
     #  - the tiny AdaLN case (64 x 256);
@@ -923,6 +982,22 @@ def run_single(args, dev):
             w["q"], w["k"], w["v"], w["biases"], w["cos"], w["sin"], w["heads"], w["eps"], outs=outs,
             stream=stream)
         nbytes = qkv_bytes(rows, w["heads"], w["head_dim"], w["rot"])
+    elif kind == "gemm":
+        rows = args.rows or ROWS
+        ops, flops = gemm_operands(h3q, dev, stream, rows)
+        c, s = h3q.h3q_gemm_swiglu_nvfp4(*ops, stream=stream)
+        fn = lambda: h3q.h3q_gemm_swiglu_nvfp4(*ops, c, s, stream=stream)  # noqa: E731
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        _, per = time_launches(fn, args.steps, stream)
+        ms = sorted(per)[len(per) // 2]
+        tpeak, tsrc = fp4_peak()
+        tflops = flops / (ms * 1e-3) / 1e12
+        return {"kernel": kind, "rows": rows, "median_launch_ms": round(ms, 4), "tflops": round(tflops, 1),
+                "frac_of_peak": round(tflops / tpeak, 4), "peak_tflops": round(tpeak, 1), "peak_source": tsrc,
+                "flops": flops, "launches": args.steps, "warmup": args.warmup,
+                "error_flag": h3q.h3q_gemm_error_flag()}
     else:
         rows = args.rows or ROWS
         x = workloads.attention_output(dev, tokens=rows)
@@ -956,7 +1031,7 @@ def main(argv=None):
     p.add_argument("--no-extras", action="store_true", help="skip producers, e2e and cpu baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--kernel", choices=["adaln", "swiglu", "swiglu_packed", "quantize", "residual", "qkv",
-                                        "dequantize"],
+                                        "dequantize", "gemm"],
                    help="time one producer alone (for profiling); prints a short JSON line")
     p.add_argument("--rows", type=int, default=0, help="rows for --kernel (default: full size)")
     args = p.parse_args(argv)

@@ -87,7 +87,7 @@ extern "C" {
 #define H3Q_ERR_INVALID_ARGUMENT 1
 #define H3Q_ERR_CUDA 2
 
-#define H3Q_ABI_VERSION 2
+#define H3Q_ABI_VERSION 3
 
 /* Rows of the scale matrix: rows rounded up to a multiple of 128. */
 static inline int64_t h3q_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
@@ -354,6 +354,57 @@ int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, c
                      const void *cos, const void *sin, int64_t rot, int interleaved, int64_t rows,
                      int64_t heads, int64_t head_dim, float eps, void *q_out, void *k_out,
                      void *v_out, void *stream);
+
+/*
+ * The FFN-up projection as a block-scaled NVFP4 GEMM on the tensor cores, with
+ * the SwiGLU and the NVFP4 quantize of its output in the epilogue.  (FastVideo
+ * compare "fasth3-spark-exact-perf", minimax_h3_swiglu_gemm.cu:
+ * launch_gemm_swiglu -- NVFP4 A and B, value/gate-paired weight columns, alpha
+ * and the global scale as device pointers -- and h3_epilogue::Store -- value =
+ * bf16(alpha * acc), gate = bf16(alpha * acc), SwiGLU, block quantize.)
+ *
+ *   acc[i][j] = sum over k of A[i][k] * B[j][k]        (fp32, tensor-core order)
+ *   u = bf16(fl(alpha * acc[i][2j])),  g = bf16(fl(alpha * acc[i][2j + 1]))
+ *   y[i][j] = bf16(fl(fl(g * sigma(g)) * u))           (as h3q_swiglu_nvfp4)
+ * then y [m, n/2] is block-quantized with global_scale.  A element =
+ * E2M1value(code) * E4M3value(scale); the products are exact and the sum is
+ * accumulated in binary32 by the tensor cores in their own order (it
+ * approximates the exact sum; everything after acc is bit-exact arithmetic).
+ *
+ *   a_codes   uint8 [m, k/2] contiguous: the activation's E2M1 codes (as the
+ *             producers write them).  16-byte aligned.
+ *   a_scales  uint8 [h3q_padded_rows(m), k/16] in the 128x4 layout (as the
+ *             producers write them).  16-byte aligned.
+ *   b_codes   uint8 [n, k/2] contiguous, b_scales uint8 [n, k/16] in the 128x4
+ *             layout: the weight, row 2j the value and row 2j+1 the gate of
+ *             output j.  16-byte aligned.
+ *   m         rows of A, 0 <= m <= 2^31 - 128 (m = 0 is a no-op).
+ *   k         a multiple of 128, at most 2^24.   n  a multiple of 256, at most 2^24.
+ *   alpha     device fp32: the dequantization factor of the product (for
+ *             operands quantized with global scales g_A and g_B,
+ *             fl(1 / fl(g_A * g_B))).
+ *   global_scale  device fp32 gsf of the output quantize.
+ *   codes     out, [m, n/4].   scales  out, h3q_scale_bytes(m, n/2).
+ *   y         optional out, bf16 [m, n/2] (NULL: not written).
+ *   acc       optional out, fp32 [m, n]: the accumulator before alpha (NULL:
+ *             not written; for checking).
+ * Alignment: codes, scales, y and acc 16-byte aligned.  Outputs must not
+ * overlap an input or each other.  Status codes as the other calls.  The
+ * kernel keeps one CTA per SM with all 512 TMEM columns of it; its waits are
+ * bounded (2 s): if one runs out the kernel stops early, the outputs are
+ * unspecified, and h3q_gemm_error_flag reports it.
+ */
+int h3q_gemm_swiglu_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales, int64_t m, int64_t k,
+                          const uint8_t *b_codes, const uint8_t *b_scales, int64_t n,
+                          const float *alpha, const float *global_scale, uint8_t *codes,
+                          uint8_t *scales, void *y, float *acc, void *stream);
+
+/*
+ * *flag = 1 if a GEMM launch since the last call had a bounded wait run out
+ * (see h3q_gemm_swiglu_nvfp4), else 0; the flag is cleared.  Synchronous: it
+ * waits for the device.  Not on any page; a diagnostic of this library.
+ */
+int h3q_gemm_error_flag(int *flag);
 
 /*
  * h3q_rmsnorm_adaln_nvfp4 on HOST buffers: x read from host memory, codes and

@@ -25,6 +25,7 @@ __all__ = [
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
     "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
     "h3q_qkv_epilogue", "h3q_rmsnorm_adaln_nvfp4_host", "host_workspace_bytes",
+    "h3q_gemm_swiglu_nvfp4", "h3q_gemm_error_flag",
 ]
 
 H3Q_OK = 0
@@ -51,6 +52,8 @@ _SIGNATURES = {
                                      _I64, _I64, _P],
     "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _I64, _I64,
                          _I64, ctypes.c_float, _P, _P, _P, _P],
+    "h3q_gemm_swiglu_nvfp4": [_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P],
+    "h3q_gemm_error_flag": [_P],
 }
 
 _lock = threading.Lock()
@@ -544,3 +547,57 @@ def h3q_rmsnorm_adaln_nvfp4_host(x_host, gamma, mod_table, global_scale, codes_h
             workspace.data_ptr(), workspace.numel(), int(chunk_rows), _stream(stream, dev))
     _check("h3q_rmsnorm_adaln_nvfp4_host", rc)
     return codes_host, scales_host
+
+
+def h3q_gemm_swiglu_nvfp4(a_codes, a_scales, b_codes, b_scales, alpha, global_scale, codes=None, scales=None,
+                          y=None, acc=None, stream=None):
+    """The FFN-up projection as a block-scaled NVFP4 GEMM with the SwiGLU + NVFP4 epilogue.
+
+    ``a_codes`` uint8 [m, k/2] and ``a_scales`` uint8 [pad128(m), k/16] (128x4 layout) are
+    the NVFP4 activation; ``b_codes`` [n, k/2] and ``b_scales`` [n, k/16] the NVFP4 weight,
+    row 2j the value and row 2j+1 the gate of output j.  ``alpha`` and ``global_scale`` are
+    device fp32 scalars.  Outputs: codes [m, n/4], scales [pad128(m), n/32]; optional ``y``
+    (bf16 [m, n/2]) and ``acc`` (fp32 [m, n], the accumulator before alpha).
+    Returns (codes, scales).
+    """
+    import torch
+
+    _cuda_tensor("a_codes", a_codes, torch.uint8)
+    dev = a_codes.device
+    if a_codes.dim() != 2 or not a_codes.is_contiguous():
+        raise ValueError("a_codes must be contiguous [m, k/2]")
+    m, k = a_codes.shape[0], 2 * a_codes.shape[1]
+    _cuda_tensor("b_codes", b_codes, torch.uint8, dev)
+    if b_codes.dim() != 2 or b_codes.shape[1] != k // 2 or not b_codes.is_contiguous():
+        raise ValueError("b_codes must be contiguous [n, k/2]")
+    n = b_codes.shape[0]
+    f = n // 2
+    for name, t, rows in (("a_scales", a_scales, padded_rows(m)), ("b_scales", b_scales, padded_rows(n))):
+        _cuda_tensor(name, t, torch.uint8, dev)
+        if not t.is_contiguous() or t.numel() != rows * (k // 16):
+            raise ValueError(f"{name} must be contiguous with {rows} x {k // 16} bytes")
+    _gsf(alpha, dev)
+    gsf = _gsf(global_scale, dev)
+    codes, scales = _outputs(dev, m, f, codes, scales)
+    y_ptr = acc_ptr = None
+    if y is not None:
+        _contiguous("y", y, torch.bfloat16, (m, f), dev)
+        y_ptr = y.data_ptr()
+    if acc is not None:
+        _contiguous("acc", acc, torch.float32, (m, n), dev)
+        acc_ptr = acc.data_ptr()
+    with torch.cuda.device(dev):
+        rc = library().h3q_gemm_swiglu_nvfp4(
+            a_codes.data_ptr(), a_scales.data_ptr(), m, k, b_codes.data_ptr(), b_scales.data_ptr(), n,
+            alpha.data_ptr(), gsf.data_ptr(), codes.data_ptr(), scales.data_ptr(), y_ptr, acc_ptr,
+            _stream(stream, dev))
+    _check("h3q_gemm_swiglu_nvfp4", rc)
+    return codes, scales
+
+
+def h3q_gemm_error_flag() -> int:
+    """Reads and clears the flag the GEMM kernel sets when a bounded wait ran out
+    (synchronises the device); 0 when none did."""
+    flag = ctypes.c_int(0)
+    _check("h3q_gemm_error_flag", library().h3q_gemm_error_flag(ctypes.byref(flag)))
+    return flag.value

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libh3q.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "h3q.h")
 
 SOURCES = ["h3q_api.cu", "quantize.cu", "adaln.cu", "swiglu.cu", "dequantize.cu", "amax.cu",
-           "residual.cu", "qkv.cu", "host_pipeline.cu"]
+           "residual.cu", "qkv.cu", "host_pipeline.cu", "gemm_swiglu.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
                      "-Xptxas", "-v"]

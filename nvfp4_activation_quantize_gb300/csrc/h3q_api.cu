@@ -448,6 +448,51 @@ int h3q_quantize_nvfp4_dynamic(const void* x, int64_t ld_x, int64_t rows, int64_
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_gemm_swiglu_nvfp4(const uint8_t* a_codes, const uint8_t* a_scales, int64_t m, int64_t k,
+                          const uint8_t* b_codes, const uint8_t* b_scales, int64_t n, const float* alpha,
+                          const float* global_scale, uint8_t* codes, uint8_t* scales, void* y, float* acc,
+                          void* stream) {
+  static const char* fn = "h3q_gemm_swiglu_nvfp4";
+  g_last_error.clear();
+  if (m < 0) return invalid(fn, "m must be >= 0");
+  if (m > (int64_t(1) << 31) - 128) return invalid(fn, "m exceeds 2^31 - 128");
+  if (k <= 0 || k % 128 != 0 || k > kMaxCols) return invalid(fn, "k must be a positive multiple of 128, at most 2^24");
+  if (n <= 0 || n % 256 != 0 || n > kMaxCols) return invalid(fn, "n must be a positive multiple of 256, at most 2^24");
+  if (m == 0) return H3Q_OK;
+  if (a_codes == nullptr || b_codes == nullptr || a_scales == nullptr || b_scales == nullptr)
+    return invalid(fn, "a_codes, a_scales, b_codes and b_scales must not be NULL");
+  if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(a_scales, 16) || !aligned(b_scales, 16))
+    return invalid(fn, "a_codes, a_scales, b_codes and b_scales must be 16-byte aligned");
+  if (alpha == nullptr || !aligned(alpha, 4)) return invalid(fn, "alpha must be a 4-byte aligned pointer");
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  if ((y != nullptr && !aligned(y, 16)) || (acc != nullptr && !aligned(acc, 16)))
+    return invalid(fn, "y and acc must be 16-byte aligned (or NULL)");
+  const int64_t f = n / 2;
+  const Span in[] = {span(a_codes, m * (k / 2)), span(a_scales, h3q_scale_bytes(m, k)),
+                     span(b_codes, n * (k / 2)), span(b_scales, h3q_scale_bytes(n, k)), span(alpha, 4),
+                     span(global_scale, 4)};
+  const Span out[] = {span(codes, h3q_code_bytes(m, f)), span(scales, h3q_scale_bytes(m, f)),
+                      y ? span(y, m * f * 2) : Span{0, 0}, acc ? span(acc, m * n * 4) : Span{0, 0}};
+  for (int i = 0; i < 4; ++i) {
+    for (const Span& x : in)
+      if (overlap(out[i], x)) return invalid(fn, "outputs overlap an input");
+    for (int j = 0; j < i; ++j)
+      if (overlap(out[i], out[j])) return invalid(fn, "outputs overlap each other");
+  }
+  cudaError_t err = h3q::launch_gemm_swiglu(a_codes, a_scales, m, k, b_codes, b_scales, n, alpha, global_scale,
+                                            codes, scales, static_cast<uint16_t*>(y), acc,
+                                            static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
+int h3q_gemm_error_flag(int* flag) {
+  static const char* fn = "h3q_gemm_error_flag";
+  g_last_error.clear();
+  if (flag == nullptr) return invalid(fn, "flag must not be NULL");
+  cudaError_t err = h3q::gemm_error_flag(flag);
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 int h3q_swiglu_packed_nvfp4(const void* o, int64_t ld_o, const void* bias, int64_t rows,
                             int64_t f, const float* global_scale, uint8_t* codes, uint8_t* scales,
                             void* stream) {

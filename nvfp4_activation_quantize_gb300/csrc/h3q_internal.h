@@ -83,7 +83,18 @@ cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
                                 int64_t rows, int64_t heads, int64_t head_dim, float eps,
                                 cudaStream_t stream);
 
-// RMSNorm + AdaLN -> NVFP4 on host buffers (x in, codes and scales out), the
+// Block-scaled NVFP4 GEMM acc = A B^T (A [m, k], B [n, k], E2M1 codes and 128x4
+// E4M3 scales) on the tensor cores with the SwiGLU + NVFP4 epilogue: column 2j
+// of acc is the value and 2j + 1 the gate of output j.  k % 128 == 0,
+// n % 256 == 0; y (bf16 [m, n/2]) and acc (fp32 [m, n]) are optional outputs.
+cudaError_t launch_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, int64_t m, int64_t k, const uint8_t* b,
+                               const uint8_t* sfb, int64_t n, const float* alpha, const float* gsf,
+                               uint8_t* codes, uint8_t* scales, uint16_t* y, float* acc, cudaStream_t stream);
+// Reads and clears the flag a GEMM kernel sets when one of its bounded waits ran
+// out (synchronous).
+cudaError_t gemm_error_flag(int* flag);
+
+// RMSNorm + AdaLN -> NVFP4 on host buffers// RMSNorm + AdaLN -> NVFP4 on host buffers (x in, codes and scales out), the
 // copies pipelined with the producer over chunk_rows-row chunks; `workspace`
 // holds h3q_host_workspace_bytes(chunk_rows, cols, rows, row_frame == nullptr)
 // bytes of device memory (include/h3q.h), 256-byte aligned.

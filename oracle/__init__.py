@@ -498,7 +498,7 @@ def nvfp4_gemm(a_codes: np.ndarray, a_sf: np.ndarray, b_codes: np.ndarray, b_sf:
 
     def work(span):
         i0, i1 = span
-        au = np.empty(k, np.int64)
+        au = np.empty((i1 - i0) * k, np.int64)
         bu = np.empty(k, np.int64)
         lib().orc_nvfp4_gemm_rows(_ptr(a), _ptr(sfa), i0, i1, k, _ptr(b), _ptr(sfb), n, _ptr(au),
                                   _ptr(bu), _ptr(acc[i0:i1]))

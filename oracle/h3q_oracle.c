@@ -715,20 +715,21 @@ static void nvfp4_row_units(const uint8_t *codes, const uint8_t *sf, int64_t k, 
 }
 
 /* acc [m, n] (rows i0..i1 of it) of A codes [m, k/2] with logical scales
- * [m, k/16] and B codes [n, k/2] with logical scales [n, k/16].  a_units and
- * b_units are scratch of k int64 each (per row of A, of B). */
+ * [m, k/16] and B codes [n, k/2] with logical scales [n, k/16].  a_units is
+ * scratch of (i1 - i0) * k int64 (A's rows as integers), b_units of k. */
 void orc_nvfp4_gemm_rows(const uint8_t *a, const uint8_t *sfa, int64_t i0, int64_t i1, int64_t k,
                          const uint8_t *b, const uint8_t *sfb, int64_t n, int64_t *a_units,
                          int64_t *b_units, float *acc)
 {
-    /* B rows outermost: each converted once, then dotted with the block's A rows */
+    for (int64_t i = i0; i < i1; ++i)
+        nvfp4_row_units(a + i * (k / 2), sfa + i * (k / 16), k, a_units + (i - i0) * k);
     for (int64_t j = 0; j < n; ++j) {
         nvfp4_row_units(b + j * (k / 2), sfb + j * (k / 16), k, b_units);
         for (int64_t i = i0; i < i1; ++i) {
-            nvfp4_row_units(a + i * (k / 2), sfa + i * (k / 16), k, a_units);
+            const int64_t *au = a_units + (i - i0) * k;
             int64_t sum = 0;
             for (int64_t e = 0; e < k; ++e)
-                sum += a_units[e] * b_units[e];
+                sum += au[e] * b_units[e];
             acc[(i - i0) * n + j] = ldexpf((float)sum, -20);
         }
     }

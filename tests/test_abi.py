@@ -37,7 +37,7 @@ def test_header_declares_the_four_calls():
 def test_every_declared_symbol_is_exported(lib):
     for fn in _declared_functions():
         assert hasattr(lib, fn), f"{fn} is declared in h3q.h but not exported"
-    assert lib.h3q_abi_version() == 2
+    assert lib.h3q_abi_version() == 3
 
 
 def _q(lib, x=0x10000, ld=256, rows=4, cols=256, gsf=0x20000, codes=0x30000, scales=0x40000):
@@ -257,3 +257,20 @@ def test_host_call_rejects_bad_arguments_on_the_host(lib):
     assert call(codes=0x7000000 + 4096) == 1 and "overlap" in h3q.h3q_last_error()  # codes inside x
     assert call(ws=0x1000000 - 512) == 1 and "workspace" in h3q.h3q_last_error()      # workspace on gamma
     assert call(rows=0, x=None) == h3q.H3Q_OK
+
+
+def test_gemm_swiglu_host_checks_run_before_any_cuda_call():
+    """h3q_gemm_swiglu_nvfp4 rejects shapes, alignment and overlaps on the host."""
+    lib = h3q.library()
+    f = lib.h3q_gemm_swiglu_nvfp4
+    A, AS, B, BS, AL, G, C, S = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x500010, 0x600000, 0x700000
+    # (a, a_scales, m, k, b, b_scales, n, alpha, gsf, codes, scales, y, acc, stream)
+    assert f(A, AS, 4, 100, B, BS, 256, AL, G, C, S, None, None, None) == 1       # k % 128
+    assert f(A, AS, 4, 128, B, BS, 200, AL, G, C, S, None, None, None) == 1       # n % 256
+    assert f(A, AS, -1, 128, B, BS, 256, AL, G, C, S, None, None, None) == 1      # m < 0
+    assert f(A + 8, AS, 4, 128, B, BS, 256, AL, G, C, S, None, None, None) == 1   # a not 16-byte aligned
+    assert f(A, AS, 4, 128, B, BS, 256, None, G, C, S, None, None, None) == 1     # no alpha
+    assert f(A, AS, 4, 128, B, BS, 256, AL, G, C, S, C + 16, None, None) == 1     # y inside codes
+    assert "overlap" in h3q.h3q_last_error()
+    assert f(A, AS, 4, 128, B, BS, 256, AL, G, A, S, None, None, None) == 1       # codes over a
+    assert f(None, None, 0, 128, None, None, 256, None, None, None, None, None, None, None) == 0  # m = 0

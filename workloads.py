@@ -10,7 +10,8 @@ describe for MiniMax-H3 video DiT serving:
   FastVideo commit log's int64 fix: 56 x 128 per token);
 * 65,280 tokens = 32 latent frames x 2,040 tokens (544 x 960 at 16x spatial
   downsampling is 34 x 60 = 2,040 tokens per frame), row -> frame = row // 2,040;
-* FFN width 18,944 for the SwiGLU producer;
+* FFN width 18,944 for the SwiGLU producer (and the FFN-up GEMM: 7,168 ->
+  2 x 18,944, value/gate-paired weight rows);
 * 300,000 tokens for the attention output crosses 2^31 elements (the pages'
   boundary for 56 x 128 is 299,593 tokens).
 
@@ -188,6 +189,22 @@ def qkv_inputs(device, rows: int = TOKENS, heads: int = 56, head_dim: int = 128,
         sin = torch.cat([theta.sin(), theta.sin()], 1).to(torch.bfloat16)
     return {"q": q, "k": k, "v": v, "biases": biases, "cos": cos, "sin": sin, "heads": heads,
             "head_dim": head_dim, "rot": rot, "eps": 1e-6}
+
+
+def ffn_up_inputs(device, rows: int = TOKENS, hidden: int = HIDDEN, ffn: int = FFN, seed: int = 8,
+                  w_std: float | None = None) -> dict:
+    """The FFN-up projection's bf16 operands before their NVFP4 quantize: the
+    activation x [rows, hidden] ~ N(0, 1) * s_j with per-channel s_j ~
+    LogNormal(0, 0.5) (a normed, modulated hidden state), and the weight
+    w [2 * ffn, hidden] ~ N(0, w_std^2), w_std = 1 / sqrt(hidden) by default,
+    its rows interleaved as (value, gate) pairs: row 2j the value and row 2j+1
+    the gate of output j.  (Random-init weights; no checkpoint is involved.)"""
+    g = _gen(device, seed)
+    s = torch.exp(torch.randn(hidden, generator=g, device=device) * 0.5)
+    x = _normal_bf16(rows, hidden, g, device, col_scale=s)
+    std = hidden ** -0.5 if w_std is None else w_std
+    w = _normal_bf16(2 * ffn, hidden, g, device, std=std)
+    return {"x": x, "w": w}
 
 
 def sample_rows(rows: int, head: int = 256, tail: int = 256, random: int = 4096,
