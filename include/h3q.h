@@ -379,7 +379,7 @@ int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, c
  *             layout: the weight, row 2j the value and row 2j+1 the gate of
  *             output j.  16-byte aligned.
  *   m         rows of A, 0 <= m <= 2^31 - 128 (m = 0 is a no-op).
- *   k         a multiple of 128, at most 2^24.   n  a multiple of 256, at most 2^24.
+ *   k         a multiple of 256, at most 2^24.   n  a multiple of 256, at most 2^24.
  *   alpha     device fp32: the dequantization factor of the product (for
  *             operands quantized with global scales g_A and g_B,
  *             fl(1 / fl(g_A * g_B))).

@@ -13,26 +13,30 @@
 // Work: persistent CTAs, one per SM, each taking 128 x 256 tiles of acc (128
 // rows of A, 256 rows of B = 128 outputs) in a grouped order (64 row tiles of A
 // sweep all of B's column tiles), so a group's A stays in L2 while B streams.
-// Warp roles inside a CTA of 12 warps:
-//   warp 0, one lane   TMA producer: per 128-element k stage, a 2-D tensor copy
-//                      of A (128 rows x 64 bytes) and of B (256 x 64), 64-byte
-//                      swizzle, and 1-D bulk copies of the stage's scale atoms
-//                      (the 128x4 layout is the one tcgen05.cp reads), all
-//                      completing on the stage's mbarrier; six stages.
-//   warp 1             allocates the 512 TMEM columns; one lane issues, per
-//                      stage, tcgen05.cp of the scale atoms into the stage's
-//                      TMEM scale slot and two tcgen05.mma (kind::mxf4nvf4,
+// Warp roles inside a CTA of 13 warps:
+//   warp 12, one lane  TMA producer: per 256-element k stage, a 2-D tensor copy
+//                      of A (128 rows x 128 bytes) and of B (256 x 128), 128-byte
+//                      swizzle, and 1-D bulk copies of the stage's 128x4 scale
+//                      atoms, all completing on the stage's mbarrier; three
+//                      stages.
+//   warps 0..3         (warp 1 also allocates the 512 TMEM columns) per stage
+//                      write the scale atoms into the stage's TMEM scale slot
+//                      with tcgen05.st -- each thread its own TMEM lane, the
+//                      layout tcgen05.cp .32x128b.warpx4 would write, but
+//                      without occupying the tensor pipe, where those copies
+//                      took as long as the MMAs -- then, after a named barrier,
+//                      one lane issues four tcgen05.mma (kind::mxf4nvf4,
 //                      block_scale, 16-element blocks, M = 128, N = 256, K = 64)
-//                      accumulating in TMEM columns 0..255, then tcgen05.commit
+//                      accumulating in TMEM columns 0..255 and tcgen05.commit
 //                      to free the stage; after the last stage a commit tells
 //                      the epilogue the accumulator is complete.
 //   warps 4..11        the epilogue: warp w reads TMEM lane quarter w % 4 (one
 //                      accumulator row per thread) and half of the tile's
-//                      columns; per 32 columns (16 outputs) it forms value and
-//                      gate, y by the SiLU table (or directly), and the NVFP4
-//                      block of y: 8 code bytes and one scale byte, all in the
-//                      thread's own registers.  Then it frees the accumulator.
-//   warps 2, 3         help fill the tables, then wait.
+//                      columns, forms the bf16 value and gate pairs in registers
+//                      and hands the accumulator back (the next tile's MMAs
+//                      start); then per 16 outputs y by the SiLU table (or
+//                      directly) and the NVFP4 block of y: 8 code bytes and one
+//                      scale byte, all in the thread's own registers.
 // Every wait is bounded: a wait that runs out sets a device flag, tells the
 // other roles to stop, and the CTA drains what it has in flight, frees its TMEM
 // and returns (h3q_gemm_error_flag reads and clears the flag).
@@ -49,24 +53,28 @@ namespace {
 
 constexpr int kTileM = 128;                       // acc rows per tile (the MMA's M)
 constexpr int kTileN = 256;                       // acc columns per tile (the MMA's N)
-constexpr int kStageK = 128;                      // K elements per pipeline stage (64 bytes a row)
-constexpr int kStages = 6;
-constexpr int kThreads = 384;
+constexpr int kStageK = 256;                      // K elements per pipeline stage (128 bytes a row)
+constexpr int kKSteps = kStageK / 64;             // tcgen05.mma per stage (K = 64 each)
+constexpr int kStages = 3;
+constexpr int kThreads = 416;                     // 13 warps
+constexpr int kMmaThreads = 128;                  // warps 0..3: scale fill and MMA issue
 constexpr int kEpiWarp0 = 4;                      // first epilogue warp
+constexpr int kTmaWarp = 12;
 constexpr int kEpiThreads = 256;
 constexpr int kGroupM = 64;                       // row tiles of A per raster group
 
-constexpr int kABytes = kTileM * kStageK / 2;     // 8 KB
-constexpr int kBBytes = kTileN * kStageK / 2;     // 16 KB
-constexpr int kSfaBytes = 2 * 512;                // two 128x4 atoms (k blocks of 64)
-constexpr int kSfbBytes = 4 * 512;                // two row tiles x two atoms
+constexpr int kABytes = kTileM * kStageK / 2;     // 16 KB
+constexpr int kBBytes = kTileN * kStageK / 2;     // 32 KB
+constexpr int kSfaBytes = kKSteps * 512;          // one 128x4 atom per K = 64 step
+constexpr int kSfbBytes = 2 * kKSteps * 512;      // two row tiles of B x one atom per step
 constexpr uint32_t kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 
 // TMEM columns: the fp32 accumulator at 0..255, then one scale slot per stage:
-// A's scales of the stage's two K = 64 steps (4 columns each) and B's (8 each).
+// A's scales of the stage's K = 64 steps (4 columns each) and B's (8 each).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfSlot0 = 256;
-constexpr uint32_t kSfSlotCols = 24;
+constexpr uint32_t kSfSlotCols = 12 * kKSteps;
+static_assert(kSfSlot0 + kStages * kSfSlotCols <= kTmemCols, "TMEM columns");
 
 // Shared memory carve-up (offsets from a 1024-byte aligned base).
 constexpr int kOffA = 0;
@@ -191,7 +199,7 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // Shared memory matrix descriptor: start address, leading and stride byte
 // offsets (all >> 4), the descriptor version 1 at bits 46-47, the layout at
-// bits 61-63 (0 none, 4 64-byte swizzle).
+// bits 61-63 (0 none, 2 128-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint32_t layout) {
   return static_cast<uint64_t>((addr >> 4) & 0x3fffu) |
@@ -200,17 +208,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (static_cast<uint64_t>(layout) << 61);
 }
 
-// A or B stage operand: K-major rows of 64 bytes, 64-byte swizzle, 8-row groups
-// 512 bytes apart.
-__device__ __forceinline__ uint64_t operand_desc(uint32_t addr) { return smem_desc(addr, 16, 512, 4); }
-
-// One 128x4 scale atom (32 rows of 16 bytes, no swizzle, 8-row groups 128
-// bytes apart), the source of tcgen05.cp .32x128b.warpx4.
-__device__ __forceinline__ uint64_t scale_desc(uint32_t addr) { return smem_desc(addr, 16, 128, 0); }
-
-__device__ __forceinline__ void tc_copy_scales(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
+// A or B stage operand: K-major rows of 128 bytes, 128-byte swizzle, 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
                                        uint32_t accumulate) {
@@ -241,6 +241,41 @@ __device__ __forceinline__ void tc_load32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 __device__ __forceinline__ void tc_wait_load() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 and 32 consecutive 32-bit columns of this warp's TMEM lane quarter, one
+// lane per thread (the thread's own row).
+__device__ __forceinline__ void tc_store16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_store32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_store() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Named barrier 1 over the scale-fill group (warps 0..3) that returns the AND
+// of every thread's `ok`, so the group leaves its loop as one.
+__device__ __forceinline__ bool group_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u), "r"(kMmaThreads)
+      : "memory");
+  return r != 0;
+}
 
 // --- tile order ---------------------------------------------------------------------
 
@@ -308,93 +343,114 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Warps 0 and 1 run their role on one lane; the other lanes wait at the
-  // __syncwarp below so the warp reaches the final (aligned) barrier converged.
-  if (warp == 0) {
+  if (warp == kTmaWarp) {
+    // ---- TMA producer (one lane; the others wait at the __syncwarp below so the
+    // warp reaches the final, aligned barrier converged)
     if (lane == 0) {
-    // ---- TMA producer
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
-    const int64_t atoms_k = args.k / 64;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued, parity of the last issue
-    bool ok = true;
-    for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      int64_t mt, nt;
-      tile_of(t, tiles_m, tiles_n, mt, nt);
-      const uint8_t* sfa = args.sfa + mt * atoms_k * 512;
-      const uint8_t* sfb = args.sfb + nt * 2 * atoms_k * 512;
-      for (int kt = 0; kt < stages_k; ++kt) {
-        if (!(ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort))) break;
-        const uint32_t full = bar_full + 8 * stage;
-        mbar_expect_tx(full, kStageTx);
-        tma_load_2d(base + kOffA + stage * kABytes, &map_a, kt * 64, static_cast<int>(mt * kTileM), full);
-        tma_load_2d(base + kOffB + stage * kBBytes, &map_b, kt * 64, static_cast<int>(nt * kTileN), full);
-        bulk_load(base + kOffSfa + stage * kSfaBytes, sfa + kt * 2 * 512, 1024, full);
-        bulk_load(base + kOffSfb + stage * kSfbBytes, sfb + kt * 2 * 512, 1024, full);
-        bulk_load(base + kOffSfb + stage * kSfbBytes + 1024, sfb + (atoms_k + kt * 2) * 512, 1024, full);
-        issued |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+      const int64_t atoms_k = args.k / 64;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued, parity of the last issue
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        int64_t mt, nt;
+        tile_of(t, tiles_m, tiles_n, mt, nt);
+        const uint8_t* sfa = args.sfa + mt * atoms_k * 512;
+        const uint8_t* sfb = args.sfb + nt * 2 * atoms_k * 512;
+        for (int kt = 0; kt < stages_k; ++kt) {
+          if (!(ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort))) break;
+          const uint32_t full = bar_full + 8 * stage;
+          constexpr uint32_t kSfChunk = kKSteps * 512;  // one row tile's atoms of the stage
+          mbar_expect_tx(full, kStageTx);
+          tma_load_2d(base + kOffA + stage * kABytes, &map_a, kt * (kStageK / 2), static_cast<int>(mt * kTileM),
+                      full);
+          tma_load_2d(base + kOffB + stage * kBBytes, &map_b, kt * (kStageK / 2), static_cast<int>(nt * kTileN),
+                      full);
+          bulk_load(base + kOffSfa + stage * kSfaBytes, sfa + kt * kSfChunk, kSfChunk, full);
+          bulk_load(base + kOffSfb + stage * kSfbBytes, sfb + kt * kSfChunk, kSfChunk, full);
+          bulk_load(base + kOffSfb + stage * kSfbBytes + kSfChunk, sfb + atoms_k * 512 + kt * kSfChunk, kSfChunk,
+                    full);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    // Copies still in flight must land before the CTA may exit: on an abort,
-    // wait (bounded) for the last issue into every stage to complete.
-    if (!ok)
-      for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) mbar_drain(bar_full + 8 * s, (issued_parity >> s) & 1u);
+      // Copies still in flight must land before the CTA may exit: on an abort,
+      // wait (bounded) for the last issue into every stage to complete.
+      if (!ok)
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_drain(bar_full + 8 * s, (issued_parity >> s) & 1u);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-    // ---- MMA issuer
+  } else if (warp < kMmaThreads / 32) {
+    // ---- scale fill and MMA issue (warps 0..3, one TMEM lane quarter each).
+    // Per stage every thread copies its row (m mod 32) of each of the stage's 12
+    // scale atoms from shared memory into its own TMEM lane with tcgen05.st --
+    // the layout tcgen05.cp .32x128b.warpx4 would give, without taking the
+    // tensor pipe -- then the group meets at a named barrier and one lane
+    // issues the stage's MMAs.
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool issuer = threadIdx.x == 0;
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      if (!(ok = mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort))) break;
-      tc_fence_after();
       for (int kt = 0; kt < stages_k; ++kt) {
-        if (!(ok = mbar_wait(bar_full + 8 * stage, phase, abort))) break;
-        tc_fence_after();
-        const uint32_t slot = tmem + kSfSlot0 + kSfSlotCols * stage;
-        const uint32_t sfa = base + kOffSfa + stage * kSfaBytes;
-        const uint32_t sfb = base + kOffSfb + stage * kSfbBytes;
+        ok = mbar_wait(bar_full + 8 * stage, phase, abort);
+        const uint32_t slot = kSfSlot0 + kSfSlotCols * stage;
+        if (ok) {
+          tc_fence_after();
+          const uint8_t* sfa = smem + kOffSfa + stage * kSfaBytes + 16 * lane;
+          const uint8_t* sfb = smem + kOffSfb + stage * kSfbBytes + 16 * lane;
+          uint32_t va[16], vb[32];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          tc_copy_scales(slot + 4 * j, scale_desc(sfa + 512 * j));
-          tc_copy_scales(slot + 8 + 8 * j, scale_desc(sfb + 512 * j));             // rows 0..127 of B
-          tc_copy_scales(slot + 8 + 8 * j + 4, scale_desc(sfb + 1024 + 512 * j));  // rows 128..255
+          for (int j = 0; j < kKSteps; ++j) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sfa + 512 * j);
+            const uint4 y0 = *reinterpret_cast<const uint4*>(sfb + 512 * j);                 // B rows 0..127
+            const uint4 y1 = *reinterpret_cast<const uint4*>(sfb + kKSteps * 512 + 512 * j);  // rows 128..255
+            va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+            vb[8 * j] = y0.x; vb[8 * j + 1] = y0.y; vb[8 * j + 2] = y0.z; vb[8 * j + 3] = y0.w;
+            vb[8 * j + 4] = y1.x; vb[8 * j + 5] = y1.y; vb[8 * j + 6] = y1.z; vb[8 * j + 7] = y1.w;
+          }
+          // slot: A's scales of step j at columns 4j, B's at 4 * kKSteps + 8j (its
+          // rows 0..127 in the first four columns, 128..255 in the next four)
+          tc_store16(lane_base + slot, va);
+          tc_store32(lane_base + slot + 4 * kKSteps, vb);
+          tc_wait_store();
         }
-        const uint32_t a = base + kOffA + stage * kABytes;
-        const uint32_t b = base + kOffB + stage * kBBytes;
+        if (issuer && kt == 0 && ok) ok = mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort);
+        tc_fence_before();
+        if (!(ok = group_and(ok))) break;
+        if (issuer) {
+          tc_fence_after();
+          const uint32_t a = base + kOffA + stage * kABytes;
+          const uint32_t b = base + kOffB + stage * kBBytes;
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-          tc_mma(tmem, operand_desc(a + 32 * j), operand_desc(b + 32 * j), slot + 4 * j, slot + 8 + 8 * j,
-                 (kt > 0 || j > 0) ? 1u : 0u);
-        tc_commit(bar_empty + 8 * stage);  // the stage is free once these MMAs have read it
+          for (int j = 0; j < kKSteps; ++j)
+            tc_mma(tmem, operand_desc(a + 32 * j), operand_desc(b + 32 * j), tmem + slot + 4 * j,
+                   tmem + slot + 4 * kKSteps + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+          tc_commit(bar_empty + 8 * stage);  // the stage is free once these MMAs have read it
+          if (kt == stages_k - 1) tc_commit(bar_acc_full);
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (!ok) break;
-      tc_commit(bar_acc_full);
       acc_phase ^= 1u;
     }
     // On an abort, let the tcgen05 operations already issued finish before the
     // TMEM is freed (a barrier of its own; bounded).  Otherwise the epilogue's
     // wait for the last tile has already seen them all complete.
-    if (!ok) {
+    if (!ok && issuer) {
       tc_commit(bar_drain);
       mbar_drain(bar_drain, 0);
     }
-    }
-    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ---- epilogue
     const int quarter = warp & 3;
@@ -414,8 +470,11 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
       tile_of(t, tiles_m, tiles_n, mt, nt);
       const int64_t row = mt * kTileM + quarter * 32 + lane;
       const bool in_rows = row < args.m;
-      uint32_t sf_word = 0;
-#pragma unroll 1
+      // Drain: the thread's 128 accumulator columns (four blocks of 16 outputs) as
+      // bf16 value and gate pairs in registers, then the accumulator is handed
+      // back so the next tile's MMAs run while this one's SwiGLU and quantize do.
+      uint32_t uw[4][8], gw[4][8];
+#pragma unroll
       for (int bi = 0; bi < 4; ++bi) {
         const int blk = half * 4 + bi;  // 16 outputs = 32 accumulator columns
         uint32_t r[32];
@@ -427,14 +486,28 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 #pragma unroll
           for (int i = 0; i < 32; i += 4) store16(dst + i, make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]));
         }
-        Block16 ub, gb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           // outputs 2i, 2i+1: values in columns 4i, 4i+2, gates in 4i+1, 4i+3
-          ub.w[i] = float2_to_bf16x2(
+          uw[bi][i] = float2_to_bf16x2(
               mul2(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 2])), alpha2));
-          gb.w[i] = float2_to_bf16x2(
+          gw[bi][i] = float2_to_bf16x2(
               mul2(make_float2(__uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 3])), alpha2));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_acc_empty);
+      acc_phase ^= 1u;
+
+      uint32_t sf_word = 0;
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        const int blk = half * 4 + bi;
+        Block16 ub, gb;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ub.w[i] = uw[bi][i];
+          gb.w[i] = gw[bi][i];
         }
         Block16 y;
         uint32_t dw[8];
@@ -459,9 +532,6 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
       }
       // the thread's four blocks are one scale quad; rows past m (padding) get 0
       store_word(args.scales + scale_word_offset(row, nt * 2 + half, quads), sf_word);
-      tc_fence_before();
-      mbar_arrive(bar_acc_empty);
-      acc_phase ^= 1u;
     }
   }
 
@@ -494,17 +564,17 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
-// Row-major bytes [rows, row_bytes] loaded in boxes of 64 bytes x box_rows with
-// the 64-byte swizzle; rows past the end read as zero.
+// Row-major bytes [rows, row_bytes] loaded in boxes of 128 bytes x box_rows with
+// the 128-byte swizzle; rows past the end read as zero.
 cudaError_t byte_map(CUtensorMap* map, const void* p, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
   EncodeTiled enc = encode_tiled();
   if (enc == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t box[2] = {kStageK / 2, box_rows};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(p), dims, strides, box, elem,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

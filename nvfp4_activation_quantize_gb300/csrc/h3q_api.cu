@@ -456,7 +456,7 @@ int h3q_gemm_swiglu_nvfp4(const uint8_t* a_codes, const uint8_t* a_scales, int64
   g_last_error.clear();
   if (m < 0) return invalid(fn, "m must be >= 0");
   if (m > (int64_t(1) << 31) - 128) return invalid(fn, "m exceeds 2^31 - 128");
-  if (k <= 0 || k % 128 != 0 || k > kMaxCols) return invalid(fn, "k must be a positive multiple of 128, at most 2^24");
+  if (k <= 0 || k % 256 != 0 || k > kMaxCols) return invalid(fn, "k must be a positive multiple of 256, at most 2^24");
   if (n <= 0 || n % 256 != 0 || n > kMaxCols) return invalid(fn, "n must be a positive multiple of 256, at most 2^24");
   if (m == 0) return H3Q_OK;
   if (a_codes == nullptr || b_codes == nullptr || a_scales == nullptr || b_scales == nullptr)

@@ -85,7 +85,7 @@ cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
 
 // Block-scaled NVFP4 GEMM acc = A B^T (A [m, k], B [n, k], E2M1 codes and 128x4
 // E4M3 scales) on the tensor cores with the SwiGLU + NVFP4 epilogue: column 2j
-// of acc is the value and 2j + 1 the gate of output j.  k % 128 == 0,
+// of acc is the value and 2j + 1 the gate of output j.  k % 256 == 0,
 // n % 256 == 0; y (bf16 [m, n/2]) and acc (fp32 [m, n]) are optional outputs.
 cudaError_t launch_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, int64_t m, int64_t k, const uint8_t* b,
                                const uint8_t* sfb, int64_t n, const float* alpha, const float* gsf,

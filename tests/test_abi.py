@@ -265,12 +265,12 @@ def test_gemm_swiglu_host_checks_run_before_any_cuda_call():
     f = lib.h3q_gemm_swiglu_nvfp4
     A, AS, B, BS, AL, G, C, S = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x500010, 0x600000, 0x700000
     # (a, a_scales, m, k, b, b_scales, n, alpha, gsf, codes, scales, y, acc, stream)
-    assert f(A, AS, 4, 100, B, BS, 256, AL, G, C, S, None, None, None) == 1       # k % 128
-    assert f(A, AS, 4, 128, B, BS, 200, AL, G, C, S, None, None, None) == 1       # n % 256
-    assert f(A, AS, -1, 128, B, BS, 256, AL, G, C, S, None, None, None) == 1      # m < 0
-    assert f(A + 8, AS, 4, 128, B, BS, 256, AL, G, C, S, None, None, None) == 1   # a not 16-byte aligned
-    assert f(A, AS, 4, 128, B, BS, 256, None, G, C, S, None, None, None) == 1     # no alpha
-    assert f(A, AS, 4, 128, B, BS, 256, AL, G, C, S, C + 16, None, None) == 1     # y inside codes
+    assert f(A, AS, 4, 128, B, BS, 256, AL, G, C, S, None, None, None) == 1       # k % 256
+    assert f(A, AS, 4, 256, B, BS, 200, AL, G, C, S, None, None, None) == 1       # n % 256
+    assert f(A, AS, -1, 256, B, BS, 256, AL, G, C, S, None, None, None) == 1      # m < 0
+    assert f(A + 8, AS, 4, 256, B, BS, 256, AL, G, C, S, None, None, None) == 1   # a not 16-byte aligned
+    assert f(A, AS, 4, 256, B, BS, 256, None, G, C, S, None, None, None) == 1     # no alpha
+    assert f(A, AS, 4, 256, B, BS, 256, AL, G, C, S, C + 16, None, None) == 1     # y inside codes
     assert "overlap" in h3q.h3q_last_error()
-    assert f(A, AS, 4, 128, B, BS, 256, AL, G, A, S, None, None, None) == 1       # codes over a
-    assert f(None, None, 0, 128, None, None, 256, None, None, None, None, None, None, None) == 0  # m = 0
+    assert f(A, AS, 4, 256, B, BS, 256, AL, G, A, S, None, None, None) == 1       # codes over a
+    assert f(None, None, 0, 256, None, None, 256, None, None, None, None, None, None, None) == 0  # m = 0

@@ -92,7 +92,7 @@ def _gsf_of(acc_exact, alpha):
     return oracle.global_scale(float(np.abs(oracle.bf16_value(y)).max())), y
 
 
-@pytest.mark.parametrize("m,k,f", [(1, 128, 128), (5, 256, 256), (200, 384, 384), (128, 7168, 128),
+@pytest.mark.parametrize("m,k,f", [(1, 256, 128), (5, 256, 256), (200, 768, 384), (128, 7168, 128),
                                    (777, 1024, 768), (2000, 256, 512), (300, 2048, 1280)])
 def test_every_output_against_the_oracle(dev, m, k, f):
     a_codes, a_sf, b_codes, b_sf, alpha = _operands(dev, m, k, f, seed=m + k + f)
