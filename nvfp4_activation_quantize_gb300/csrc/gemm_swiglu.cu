@@ -13,21 +13,21 @@
 // Work: persistent CTAs, one per SM, each taking 128 x 256 tiles of acc (128
 // rows of A, 256 rows of B = 128 outputs) in a grouped order (64 row tiles of A
 // sweep all of B's column tiles), so a group's A stays in L2 while B streams.
-// Warp roles inside a CTA of 13 warps:
+// Warp roles inside a CTA of 14 warps:
 //   warp 12, one lane  TMA producer: per 256-element k stage, a 2-D tensor copy
 //                      of A (128 rows x 128 bytes) and of B (256 x 128), 128-byte
 //                      swizzle, and 1-D bulk copies of the stage's 128x4 scale
 //                      atoms, all completing on the stage's mbarrier; three
 //                      stages.
-//   warps 0..3         (warp 1 also allocates the 512 TMEM columns) per stage
-//                      write the scale atoms into the stage's TMEM scale slot
-//                      with tcgen05.st -- each thread its own TMEM lane, the
-//                      layout tcgen05.cp .32x128b.warpx4 would write, but
-//                      without occupying the tensor pipe, where those copies
-//                      took as long as the MMAs -- then, after a named barrier,
-//                      one lane issues four tcgen05.mma (kind::mxf4nvf4,
+//   warps 0..3         (warp 1 also allocates the 512 TMEM columns) write each
+//                      stage's scale atoms into the stage's TMEM scale slot with
+//                      tcgen05.st -- each thread its own TMEM lane, the layout
+//                      tcgen05.cp .32x128b.warpx4 would write, but without
+//                      occupying the tensor pipe, where those copies took as
+//                      long as the MMAs -- and signal the stage ready.
+//   warp 13, one lane  issues four tcgen05.mma per stage (kind::mxf4nvf4,
 //                      block_scale, 16-element blocks, M = 128, N = 256, K = 64)
-//                      accumulating in TMEM columns 0..255 and tcgen05.commit
+//                      accumulating in TMEM columns 0..255, and tcgen05.commit
 //                      to free the stage; after the last stage a commit tells
 //                      the epilogue the accumulator is complete.
 //   warps 4..11        the epilogue: warp w reads TMEM lane quarter w % 4 (one
@@ -56,10 +56,11 @@ constexpr int kTileN = 256;                       // acc columns per tile (the M
 constexpr int kStageK = 256;                      // K elements per pipeline stage (128 bytes a row)
 constexpr int kKSteps = kStageK / 64;             // tcgen05.mma per stage (K = 64 each)
 constexpr int kStages = 3;
-constexpr int kThreads = 416;                     // 13 warps
-constexpr int kMmaThreads = 128;                  // warps 0..3: scale fill and MMA issue
+constexpr int kThreads = 448;                     // 14 warps
+constexpr int kSfThreads = 128;                   // warps 0..3: the scale fill
 constexpr int kEpiWarp0 = 4;                      // first epilogue warp
 constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr int kEpiThreads = 256;
 constexpr int kGroupM = 64;                       // row tiles of A per raster group
 
@@ -84,7 +85,7 @@ constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr int kOffSilu = kOffSfb + kStages * kSfbBytes;
 constexpr int kOffInv = kOffSilu + 2 * kTabHalf * 4;
 constexpr int kOffBar = kOffInv + 128 * 4;
-constexpr int kBars = 2 * kStages + 3;            // full[], empty[], acc_full, acc_empty, drain
+constexpr int kBars = 3 * kStages + 3;            // full[], empty[], sf_ready[], acc_full, acc_empty, drain
 constexpr int kOffMisc = kOffBar + kBars * 8;     // TMEM base address, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -264,19 +265,6 @@ __device__ __forceinline__ void tc_store32(uint32_t taddr, const uint32_t (&v)[3
 }
 __device__ __forceinline__ void tc_wait_store() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Named barrier 1 over the scale-fill group (warps 0..3) that returns the AND
-// of every thread's `ok`, so the group leaves its loop as one.
-__device__ __forceinline__ bool group_and(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(ok ? 1u : 0u), "r"(kMmaThreads)
-      : "memory");
-  return r != 0;
-}
-
 // --- tile order ---------------------------------------------------------------------
 
 // Tile t of the grouped order: groups of kGroupM row tiles of A; inside a group
@@ -303,7 +291,8 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
   const uint32_t base = smem_u32(smem);
   const uint32_t bar_full = base + kOffBar;                 // + 8 * stage
   const uint32_t bar_empty = bar_full + 8 * kStages;        // + 8 * stage
-  const uint32_t bar_acc_full = bar_empty + 8 * kStages;
+  const uint32_t bar_sf = bar_empty + 8 * kStages;          // + 8 * stage
+  const uint32_t bar_acc_full = bar_sf + 8 * kStages;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_empty + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -322,6 +311,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, kSfThreads);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kEpiThreads);
@@ -387,70 +377,89 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
           if (issued & (1u << s)) mbar_drain(bar_full + 8 * s, (issued_parity >> s) & 1u);
     }
     __syncwarp();
-  } else if (warp < kMmaThreads / 32) {
-    // ---- scale fill and MMA issue (warps 0..3, one TMEM lane quarter each).
-    // Per stage every thread copies its row (m mod 32) of each of the stage's 12
-    // scale atoms from shared memory into its own TMEM lane with tcgen05.st --
-    // the layout tcgen05.cp .32x128b.warpx4 would give, without taking the
-    // tensor pipe -- then the group meets at a named barrier and one lane
-    // issues the stage's MMAs.
+  } else if (warp < kSfThreads / 32) {
+    // ---- scale fill (warps 0..3, one TMEM lane quarter each).  Per stage every
+    // thread copies its row (m mod 32) of each of the stage's 12 scale atoms from
+    // shared memory into its own TMEM lane with tcgen05.st -- the layout
+    // tcgen05.cp .32x128b.warpx4 would write, without taking the tensor pipe --
+    // and arrives on the stage's sf_ready barrier.  It runs up to kStages stages
+    // ahead of the MMAs: a stage's slot is rewritten only after its full barrier
+    // completes again, which needs the MMAs that read the slot to have finished.
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const bool issuer = threadIdx.x == 0;
     int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+      bool ok = true;
       for (int kt = 0; kt < stages_k; ++kt) {
-        ok = mbar_wait(bar_full + 8 * stage, phase, abort);
+        // one decision per warp (tcgen05.st is warp-aligned)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * stage, phase, abort)))) break;
+        tc_fence_after();
         const uint32_t slot = kSfSlot0 + kSfSlotCols * stage;
-        if (ok) {
-          tc_fence_after();
-          const uint8_t* sfa = smem + kOffSfa + stage * kSfaBytes + 16 * lane;
-          const uint8_t* sfb = smem + kOffSfb + stage * kSfbBytes + 16 * lane;
-          uint32_t va[16], vb[32];
+        const uint8_t* sfa = smem + kOffSfa + stage * kSfaBytes + 16 * lane;
+        const uint8_t* sfb = smem + kOffSfb + stage * kSfbBytes + 16 * lane;
+        uint32_t va[16], vb[32];
 #pragma unroll
-          for (int j = 0; j < kKSteps; ++j) {
-            const uint4 x = *reinterpret_cast<const uint4*>(sfa + 512 * j);
-            const uint4 y0 = *reinterpret_cast<const uint4*>(sfb + 512 * j);                 // B rows 0..127
-            const uint4 y1 = *reinterpret_cast<const uint4*>(sfb + kKSteps * 512 + 512 * j);  // rows 128..255
-            va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
-            vb[8 * j] = y0.x; vb[8 * j + 1] = y0.y; vb[8 * j + 2] = y0.z; vb[8 * j + 3] = y0.w;
-            vb[8 * j + 4] = y1.x; vb[8 * j + 5] = y1.y; vb[8 * j + 6] = y1.z; vb[8 * j + 7] = y1.w;
-          }
-          // slot: A's scales of step j at columns 4j, B's at 4 * kKSteps + 8j (its
-          // rows 0..127 in the first four columns, 128..255 in the next four)
-          tc_store16(lane_base + slot, va);
-          tc_store32(lane_base + slot + 4 * kKSteps, vb);
-          tc_wait_store();
+        for (int j = 0; j < kKSteps; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sfa + 512 * j);
+          const uint4 y0 = *reinterpret_cast<const uint4*>(sfb + 512 * j);                 // B rows 0..127
+          const uint4 y1 = *reinterpret_cast<const uint4*>(sfb + kKSteps * 512 + 512 * j);  // rows 128..255
+          va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+          vb[8 * j] = y0.x; vb[8 * j + 1] = y0.y; vb[8 * j + 2] = y0.z; vb[8 * j + 3] = y0.w;
+          vb[8 * j + 4] = y1.x; vb[8 * j + 5] = y1.y; vb[8 * j + 6] = y1.z; vb[8 * j + 7] = y1.w;
         }
-        if (issuer && kt == 0 && ok) ok = mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort);
+        // slot: A's scales of step j at columns 4j, B's at 4 * kKSteps + 8j (its
+        // rows 0..127 in the first four columns, 128..255 in the next four)
+        tc_store16(lane_base + slot, va);
+        tc_store32(lane_base + slot + 4 * kKSteps, vb);
+        tc_wait_store();
         tc_fence_before();
-        if (!(ok = group_and(ok))) break;
-        if (issuer) {
-          tc_fence_after();
-          const uint32_t a = base + kOffA + stage * kABytes;
-          const uint32_t b = base + kOffB + stage * kBBytes;
-#pragma unroll
-          for (int j = 0; j < kKSteps; ++j)
-            tc_mma(tmem, operand_desc(a + 32 * j), operand_desc(b + 32 * j), tmem + slot + 4 * j,
-                   tmem + slot + 4 * kKSteps + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
-          tc_commit(bar_empty + 8 * stage);  // the stage is free once these MMAs have read it
-          if (kt == stages_k - 1) tc_commit(bar_acc_full);
-        }
+        mbar_arrive(bar_sf + 8 * stage);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      acc_phase ^= 1u;
+      if (!ok) break;
     }
-    // On an abort, let the tcgen05 operations already issued finish before the
-    // TMEM is freed (a barrier of its own; bounded).  Otherwise the epilogue's
-    // wait for the last tile has already seen them all complete.
-    if (!ok && issuer) {
-      tc_commit(bar_drain);
-      mbar_drain(bar_drain, 0);
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issue (one lane)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        if (!(ok = mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort))) break;
+        tc_fence_after();
+        for (int kt = 0; kt < stages_k; ++kt) {
+          // the stage's operands are in shared memory once its scales are in TMEM
+          if (!(ok = mbar_wait(bar_sf + 8 * stage, phase, abort))) break;
+          tc_fence_after();
+          const uint32_t slot = tmem + kSfSlot0 + kSfSlotCols * stage;
+          const uint32_t a = base + kOffA + stage * kABytes;
+          const uint32_t b = base + kOffB + stage * kBBytes;
+#pragma unroll
+          for (int j = 0; j < kKSteps; ++j)
+            tc_mma(tmem, operand_desc(a + 32 * j), operand_desc(b + 32 * j), slot + 4 * j,
+                   slot + 4 * kKSteps + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
+          tc_commit(bar_empty + 8 * stage);  // the stage is free once these MMAs have read it
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar_acc_full);
+        acc_phase ^= 1u;
+      }
+      // On an abort, let the tcgen05 operations already issued finish before the
+      // TMEM is freed (a barrier of its own; bounded).  Otherwise the epilogue's
+      // wait for the last tile has already seen them all complete.
+      if (!ok) {
+        tc_commit(bar_drain);
+        mbar_drain(bar_drain, 0);
+      }
     }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ---- epilogue
     const int quarter = warp & 3;
