@@ -10,9 +10,12 @@
 // swizzled scale store.  That kernel is a CUTLASS SM120 collective; this one is
 // written for sm_103a directly.)
 //
-// Work: persistent CTAs, one per SM, each taking 128 x 256 tiles of acc (128
-// rows of A, 256 rows of B = 128 outputs) in a grouped order (64 row tiles of A
-// sweep all of B's column tiles), so a group's A stays in L2 while B streams.
+// Work: persistent CTAs, one per SM, in clusters of two on neighbouring 128-row
+// tiles of A that share one 256-row tile of B (128 outputs): each CTA loads half
+// of B's tile and of its scales with a cluster multicast into both CTAs'
+// shared memory, so a CTA moves a third fewer bytes from L2 than alone.  Units
+// go in a grouped order (32 row-tile pairs sweep all of B's column tiles), so a
+// group's A stays in L2 while B streams.
 // Warp roles inside a CTA of 14 warps:
 //   warp 12, one lane  TMA producer: per 256-element k stage, a 2-D tensor copy
 //                      of A (128 rows x 128 bytes) and of B (256 x 128), 128-byte
@@ -55,14 +58,15 @@ constexpr int kTileM = 128;                       // acc rows per tile (the MMA'
 constexpr int kTileN = 256;                       // acc columns per tile (the MMA's N)
 constexpr int kStageK = 256;                      // K elements per pipeline stage (128 bytes a row)
 constexpr int kKSteps = kStageK / 64;             // tcgen05.mma per stage (K = 64 each)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 448;                     // 14 warps
 constexpr int kSfThreads = 128;                   // warps 0..3: the scale fill
 constexpr int kEpiWarp0 = 4;                      // first epilogue warp
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kEpiThreads = 256;
-constexpr int kGroupM = 64;                       // row tiles of A per raster group
+constexpr int kCluster = 2;                       // CTAs per cluster, on neighbouring row tiles
+constexpr int kGroupPairs = 32;                   // row-tile pairs of A per raster group
 
 constexpr int kABytes = kTileM * kStageK / 2;     // 16 KB
 constexpr int kBBytes = kTileN * kStageK / 2;     // 32 KB
@@ -82,8 +86,7 @@ constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffSfa = kOffB + kStages * kBBytes;
 constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr int kOffSilu = kOffSfb + kStages * kSfbBytes;
-constexpr int kOffInv = kOffSilu + 2 * kTabHalf * 4;
+constexpr int kOffInv = kOffSfb + kStages * kSfbBytes;
 constexpr int kOffBar = kOffInv + 128 * 4;
 constexpr int kBars = 3 * kStages + 3;            // full[], empty[], sf_ready[], acc_full, acc_empty, drain
 constexpr int kOffMisc = kOffBar + kBars * 8;     // TMEM base address, abort flag
@@ -112,7 +115,16 @@ struct GemmArgs {
   uint8_t* scales;       // [pad128(m), n/32], 128x4 layout
   uint16_t* y;           // optional bf16 [m, n/2]
   float* acc;            // optional fp32 [m, n]
+  const float* silu;     // the SiLU table (g_silu_table), filled on the stream before the launch
 };
+
+// s = fl(g * sigma(g)) of every bf16 gate in the SiLU table's window (h3q_silu.cuh),
+// 32 KB: shared memory is taken by the operand stages, so the table lives here
+// (read through L1) and silu_table_kernel writes it before each GEMM launch on
+// the same stream -- the same values every time.
+__device__ __align__(16) float g_silu_table[2 * kTabHalf];
+
+__global__ void __launch_bounds__(1024) silu_table_kernel(float* table) { fill_silu_table(table); }
 
 // --- PTX wrappers ---------------------------------------------------------------
 
@@ -184,6 +196,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same copy delivered to every CTA of the cluster (same shared-memory offset
+// and the same barrier offset in each).
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
+
+__device__ __forceinline__ void tma_load_2d_all(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(kClusterMask)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_all(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(kClusterMask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -228,6 +270,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// Arrives on the barrier at this offset in every CTA of the cluster once the
+// issued tcgen05 operations have completed.
+__device__ __forceinline__ void tc_commit_all(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(kClusterMask)
+      : "memory");
+}
+
 // 32 consecutive fp32 columns of this warp's TMEM lane quarter, one row per thread.
 __device__ __forceinline__ void tc_load32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -267,23 +318,23 @@ __device__ __forceinline__ void tc_wait_store() { asm volatile("tcgen05.wait::st
 
 // --- tile order ---------------------------------------------------------------------
 
-// Tile t of the grouped order: groups of kGroupM row tiles of A; inside a group
-// the row tile varies fastest, so CTAs working at the same time share B's tile
-// and the group's A stays in L2 while B's column tiles go by.
-__device__ __forceinline__ void tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t& mt,
-                                        int64_t& nt) {
-  const int64_t per_group = int64_t{kGroupM} * tiles_n;
-  const int64_t group = t / per_group;
-  const int64_t rest = t - group * per_group;
-  const int64_t first = group * kGroupM;
-  const int64_t rows = tiles_m - first < kGroupM ? tiles_m - first : kGroupM;
-  mt = first + rest % rows;
+// Unit u of the grouped order: a pair of neighbouring row tiles of A (one per
+// CTA of the cluster) and one column tile of B.  Groups of kGroupPairs pairs;
+// inside a group the pair varies fastest, so clusters working at the same time
+// share B's tile and the group's A stays in L2 while B's column tiles go by.
+__device__ __forceinline__ void unit_of(int64_t u, int64_t pairs, int64_t tiles_n, int64_t& mp, int64_t& nt) {
+  const int64_t per_group = int64_t{kGroupPairs} * tiles_n;
+  const int64_t group = u / per_group;
+  const int64_t rest = u - group * per_group;
+  const int64_t first = group * kGroupPairs;
+  const int64_t rows = pairs - first < kGroupPairs ? pairs - first : kGroupPairs;
+  mp = first + rest % rows;
   nt = rest / rows;
 }
 
 // --- the kernel ---------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -297,20 +348,27 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
   const uint32_t bar_drain = bar_acc_empty + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  float* silu_table = reinterpret_cast<float*>(smem + kOffSilu);
   float* inv_table = reinterpret_cast<float*>(smem + kOffInv);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Work: units of (row-tile pair, column tile); this CTA takes row tile
+  // 2 * pair + rank of each unit of its cluster.  With an odd number of row
+  // tiles the last pair's second tile lies past the matrix: its A reads as zero
+  // and its outputs are not stored.
+  const uint32_t rank = cluster_rank();
+  const int64_t cluster = blockIdx.x / kCluster;
+  const int64_t clusters = gridDim.x / kCluster;
   const int64_t tiles_m = (args.m + kTileM - 1) / kTileM;
+  const int64_t pairs = (tiles_m + kCluster - 1) / kCluster;
   const int64_t tiles_n = args.n / kTileN;
-  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t units = pairs * tiles_n;
   const int stages_k = static_cast<int>(args.k / kStageK);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kCluster);  // both CTAs' MMAs must be done with the stage
       mbar_init(bar_sf + 8 * s, kSfThreads);
     }
     mbar_init(bar_acc_full, 1);
@@ -327,9 +385,9 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
   }
   const float gsf = *args.gsf;
   fill_inverse_scales(inv_table, gsf);
-  fill_silu_table(silu_table);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the partner's barriers are initialised before any copy lands in them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -344,11 +402,14 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per stage: ever issued, parity of the last issue
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        int64_t mt, nt;
-        tile_of(t, tiles_m, tiles_n, mt, nt);
-        const uint8_t* sfa = args.sfa + mt * atoms_k * 512;
-        const uint8_t* sfb = args.sfb + nt * 2 * atoms_k * 512;
+      for (int64_t u = cluster; u < units && ok; u += clusters) {
+        int64_t mp, nt;
+        unit_of(u, pairs, tiles_n, mp, nt);
+        const int64_t mt = mp * kCluster + rank;
+        const int64_t mt_sf = mt < tiles_m ? mt : tiles_m - 1;  // a phantom tile reads real scales
+        const uint8_t* sfa = args.sfa + mt_sf * atoms_k * 512;
+        // this CTA's share of B: rows 128 * rank .. of the column tile, and their scales
+        const uint8_t* sfb = args.sfb + (nt * 2 + rank) * atoms_k * 512;
         for (int kt = 0; kt < stages_k; ++kt) {
           if (!(ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort))) break;
           const uint32_t full = bar_full + 8 * stage;
@@ -356,12 +417,10 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
           mbar_expect_tx(full, kStageTx);
           tma_load_2d(base + kOffA + stage * kABytes, &map_a, kt * (kStageK / 2), static_cast<int>(mt * kTileM),
                       full);
-          tma_load_2d(base + kOffB + stage * kBBytes, &map_b, kt * (kStageK / 2), static_cast<int>(nt * kTileN),
-                      full);
           bulk_load(base + kOffSfa + stage * kSfaBytes, sfa + kt * kSfChunk, kSfChunk, full);
-          bulk_load(base + kOffSfb + stage * kSfbBytes, sfb + kt * kSfChunk, kSfChunk, full);
-          bulk_load(base + kOffSfb + stage * kSfbBytes + kSfChunk, sfb + atoms_k * 512 + kt * kSfChunk, kSfChunk,
-                    full);
+          tma_load_2d_all(base + kOffB + stage * kBBytes + rank * (kBBytes / kCluster), &map_b, kt * (kStageK / 2),
+                          static_cast<int>(nt * kTileN + rank * (kTileN / kCluster)), full);
+          bulk_load_all(base + kOffSfb + stage * kSfbBytes + rank * kSfChunk, sfb + kt * kSfChunk, kSfChunk, full);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -370,11 +429,14 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
           }
         }
       }
-      // Copies still in flight must land before the CTA may exit: on an abort,
-      // wait (bounded) for the last issue into every stage to complete.
-      if (!ok)
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) mbar_drain(bar_full + 8 * s, (issued_parity >> s) & 1u);
+      // Before the cluster may exit: every stage's last use must be released by
+      // both CTAs' MMAs (their commits arrive on this CTA's empty barriers), and on
+      // an abort every copy issued must have landed (bounded waits).
+      for (int s = 0; s < kStages; ++s) {
+        if (!(issued & (1u << s))) continue;
+        if (!ok) mbar_drain(bar_full + 8 * s, (issued_parity >> s) & 1u);
+        mbar_drain(bar_empty + 8 * s, (issued_parity >> s) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp < kSfThreads / 32) {
@@ -388,7 +450,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int64_t u = cluster; u < units; u += clusters) {
       bool ok = true;
       for (int kt = 0; kt < stages_k; ++kt) {
         // one decision per warp (tcgen05.st is warp-aligned)
@@ -427,7 +489,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int64_t u = cluster; u < units && ok; u += clusters) {
         if (!(ok = mbar_wait(bar_acc_empty, acc_phase ^ 1u, abort))) break;
         tc_fence_after();
         for (int kt = 0; kt < stages_k; ++kt) {
@@ -441,7 +503,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
           for (int j = 0; j < kKSteps; ++j)
             tc_mma(tmem, operand_desc(a + 32 * j), operand_desc(b + 32 * j), slot + 4 * j,
                    slot + 4 * kKSteps + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
-          tc_commit(bar_empty + 8 * stage);  // the stage is free once these MMAs have read it
+          tc_commit_all(bar_empty + 8 * stage);  // both CTAs: this CTA's MMAs are done with the stage
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -468,15 +530,16 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const int64_t quads = f / 64;
     const float alpha = *args.alpha;
     const float2 alpha2 = make_float2(alpha, alpha);
-    const char* table = reinterpret_cast<const char*>(silu_table);
+    const char* table = reinterpret_cast<const char*>(args.silu);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    for (int64_t u = cluster; u < units; u += clusters) {
       // one decision per warp: lanes could see an abort and the barrier at different polls
       if (!__all_sync(0xffffffffu, mbar_wait(bar_acc_full, acc_phase, abort))) break;
       tc_fence_after();
-      int64_t mt, nt;
-      tile_of(t, tiles_m, tiles_n, mt, nt);
+      int64_t mp, nt;
+      unit_of(u, pairs, tiles_n, mp, nt);
+      const int64_t mt = mp * kCluster + rank;
       const int64_t row = mt * kTileM + quarter * 32 + lane;
       const bool in_rows = row < args.m;
       // Drain: the thread's 128 accumulator columns (four blocks of 16 outputs) as
@@ -540,7 +603,8 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         }
       }
       // the thread's four blocks are one scale quad; rows past m (padding) get 0
-      store_word(args.scales + scale_word_offset(row, nt * 2 + half, quads), sf_word);
+      if (mt < tiles_m)  // a phantom row tile has no scale rows
+        store_word(args.scales + scale_word_offset(row, nt * 2 + half, quads), sf_word);
     }
   }
 
@@ -551,6 +615,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
   }
+  cluster_sync();  // no copy or commit of the partner may still be headed for this CTA
 }
 
 // --- host side ----------------------------------------------------------------------
@@ -588,6 +653,35 @@ cudaError_t byte_map(CUtensorMap* map, const void* p, int64_t rows, int64_t row_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Clusters of kCluster CTAs that fit the GPU at once (one CTA per SM), per CUDA
+// context; the first query also raises the kernel's shared-memory limit.
+cudaError_t resident_clusters(int* clusters) {
+  static std::mutex mu;
+  static unsigned long long cached_context = 0;
+  static int cached = 0;
+  unsigned long long context = 0;
+  cudaError_t err = current_context_id(&context);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  if (context != cached_context || cached == 0) {
+    const void* kernel = reinterpret_cast<const void*>(&gemm_swiglu_kernel);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};  // the cluster size is the kernel's own (__cluster_dims__)
+    cfg.gridDim = dim3(kCluster, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    cached = n;
+    cached_context = context;
+  }
+  *clusters = cached;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, int64_t m, int64_t k, const uint8_t* b,
@@ -595,15 +689,19 @@ cudaError_t launch_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, int64_t m, 
                                uint8_t* codes, uint8_t* scales, uint16_t* y, float* acc, cudaStream_t stream) {
   CUtensorMap map_a, map_b;
   cudaError_t err = byte_map(&map_a, a, m, k / 2, kTileM);
-  if (err == cudaSuccess) err = byte_map(&map_b, b, n, k / 2, kTileN);
+  if (err == cudaSuccess) err = byte_map(&map_b, b, n, k / 2, kTileN / kCluster);  // each CTA loads half
   if (err != cudaSuccess) return err;
-  const int64_t tiles = (m + kTileM - 1) / kTileM * (n / kTileN);
-  int blocks = 0;
-  err = persistent_blocks(reinterpret_cast<const void*>(&gemm_swiglu_kernel), kThreads, kSmemBytes, tiles,
-                          &blocks);
+  const int64_t units = ((m + kTileM - 1) / kTileM + kCluster - 1) / kCluster * (n / kTileN);
+  int clusters = 0;
+  err = resident_clusters(&clusters);
   if (err != cudaSuccess) return err;
-  const GemmArgs args{sfa, sfb, m, n, k, alpha, gsf, codes, scales, y, acc};
-  gemm_swiglu_kernel<<<blocks, kThreads, kSmemBytes, stream>>>(map_a, map_b, args);
+  const int64_t grid = (units < clusters ? units : clusters) * kCluster;
+  void* silu = nullptr;
+  if ((err = cudaGetSymbolAddress(&silu, g_silu_table)) != cudaSuccess) return err;
+  silu_table_kernel<<<1, 1024, 0, stream>>>(static_cast<float*>(silu));
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const GemmArgs args{sfa, sfb, m, n, k, alpha, gsf, codes, scales, y, acc, static_cast<const float*>(silu)};
+  gemm_swiglu_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
 }
 
