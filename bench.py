@@ -746,7 +746,7 @@ def measure_producers(h3q, dev, stream, args):
         "bound": "tensor", "tflops": round(tflops, 1), "peak_tflops": round(tpeak, 1), "peak_source": tsrc,
         "frac_of_peak": round(tflops / tpeak, 4), "frac_of_nominal_13_5_pf": round(tflops / 13500.0, 4),
         "median_launch_ms": round(ms, 4), "flops": flops, "rows_per_s": round(ROWS / (ms * 1e-3)),
-        "launches": len(per), "error_flag": h3q.h3q_gemm_error_flag()}
+        "launches": len(per), "error_flag": h3q.h3q_kernel_error_flag()}
     del ops, c, s
     torch.cuda.empty_cache()
 
@@ -997,7 +997,7 @@ def run_single(args, dev):
         return {"kernel": kind, "rows": rows, "median_launch_ms": round(ms, 4), "tflops": round(tflops, 1),
                 "frac_of_peak": round(tflops / tpeak, 4), "peak_tflops": round(tpeak, 1), "peak_source": tsrc,
                 "flops": flops, "launches": args.steps, "warmup": args.warmup,
-                "error_flag": h3q.h3q_gemm_error_flag()}
+                "error_flag": h3q.h3q_kernel_error_flag()}
     else:
         rows = args.rows or ROWS
         x = workloads.attention_output(dev, tokens=rows)

@@ -392,7 +392,7 @@ int h3q_qkv_epilogue(const void *q, int64_t ld_q, const void *k, int64_t ld_k, c
  * overlap an input or each other.  Status codes as the other calls.  The
  * kernel keeps one CTA per SM with all 512 TMEM columns of it; its waits are
  * bounded (2 s): if one runs out the kernel stops early, the outputs are
- * unspecified, and h3q_gemm_error_flag reports it.
+ * unspecified, and h3q_kernel_error_flag reports it.
  */
 int h3q_gemm_swiglu_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales, int64_t m, int64_t k,
                           const uint8_t *b_codes, const uint8_t *b_scales, int64_t n,
@@ -400,11 +400,13 @@ int h3q_gemm_swiglu_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales, int64
                           uint8_t *scales, void *y, float *acc, void *stream);
 
 /*
- * *flag = 1 if a GEMM launch since the last call had a bounded wait run out
- * (see h3q_gemm_swiglu_nvfp4), else 0; the flag is cleared.  Synchronous: it
- * waits for the device.  Not on any page; a diagnostic of this library.
+ * *flag = 1 if a kernel launched since the last call had one of its bounded
+ * waits run out, else 0; the flag is cleared.  The kernel that waits on
+ * mbarriers (the GEMM of h3q_gemm_swiglu_nvfp4) bounds every wait (2 s) and then
+ * stops early, leaving that call's outputs unspecified.  Synchronous: it waits
+ * for the device.  Not on any page; a diagnostic of this library.
  */
-int h3q_gemm_error_flag(int *flag);
+int h3q_kernel_error_flag(int *flag);
 
 /*
  * h3q_rmsnorm_adaln_nvfp4 on HOST buffers: x read from host memory, codes and

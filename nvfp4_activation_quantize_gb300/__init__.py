@@ -25,7 +25,7 @@ __all__ = [
     "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
     "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
     "h3q_qkv_epilogue", "h3q_rmsnorm_adaln_nvfp4_host", "host_workspace_bytes",
-    "h3q_gemm_swiglu_nvfp4", "h3q_gemm_error_flag",
+    "h3q_gemm_swiglu_nvfp4", "h3q_kernel_error_flag",
 ]
 
 H3Q_OK = 0
@@ -53,7 +53,7 @@ _SIGNATURES = {
     "h3q_qkv_epilogue": [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _I64, _I64,
                          _I64, ctypes.c_float, _P, _P, _P, _P],
     "h3q_gemm_swiglu_nvfp4": [_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P],
-    "h3q_gemm_error_flag": [_P],
+    "h3q_kernel_error_flag": [_P],
 }
 
 _lock = threading.Lock()
@@ -595,9 +595,9 @@ def h3q_gemm_swiglu_nvfp4(a_codes, a_scales, b_codes, b_scales, alpha, global_sc
     return codes, scales
 
 
-def h3q_gemm_error_flag() -> int:
-    """Reads and clears the flag the GEMM kernel sets when a bounded wait ran out
+def h3q_kernel_error_flag() -> int:
+    """Reads and clears the flag a kernel sets when one of its bounded waits ran out
     (synchronises the device); 0 when none did."""
     flag = ctypes.c_int(0)
-    _check("h3q_gemm_error_flag", library().h3q_gemm_error_flag(ctypes.byref(flag)))
+    _check("h3q_kernel_error_flag", library().h3q_kernel_error_flag(ctypes.byref(flag)))
     return flag.value

@@ -42,11 +42,12 @@
 //                      scale byte, all in the thread's own registers.
 // Every wait is bounded: a wait that runs out sets a device flag, tells the
 // other roles to stop, and the CTA drains what it has in flight, frees its TMEM
-// and returns (h3q_gemm_error_flag reads and clears the flag).
+// and returns (h3q_kernel_error_flag reads and clears the flag).
 #include <cuda.h>  // CUtensorMap; the encode function is fetched at run time
 
 #include <mutex>
 
+#include "h3q_async.cuh"
 #include "h3q_device.cuh"
 #include "h3q_internal.h"
 #include "h3q_silu.cuh"
@@ -100,9 +101,8 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (uint32_t(kTileN >> 3) << 17) |
                             (uint32_t(kTileM >> 4) << 24);
 
-constexpr uint64_t kWaitNs = 2000000000ull;       // a wait gives up after 2 s
 
-// Set when a bounded wait ran out (read and cleared by h3q_gemm_error_flag).
+// Set when a bounded wait ran out (read and cleared by h3q_kernel_error_flag).
 __device__ int g_gemm_fault;
 
 struct GemmArgs {
@@ -128,45 +128,11 @@ __global__ void __launch_bounds__(1024) silu_table_kernel(float* table) { fill_s
 
 // --- PTX wrappers ---------------------------------------------------------------
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Wait for the phase of parity `parity` of the barrier to complete.  Gives up
 // (false) when another role has raised the abort flag, or after kWaitNs, which
 // raises it and the device fault flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;  // the common case, without reading the timer
   const uint64_t start = now_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -181,11 +147,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // The same wait with no abort flag (the drain after an abort), bounded the same way.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t start = now_ns();
-  for (uint32_t i = 1; !mbar_try_wait(bar, parity); ++i)
-    if ((i & 255u) == 0 && now_ns() - start > kWaitNs) return;
-}
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) { (void)wait_bounded(bar, parity); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -226,12 +188,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -375,7 +331,7 @@ gemm_swiglu_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     mbar_init(bar_acc_empty, kEpiThreads);
     mbar_init(bar_drain, 1);
     *abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 1) {  // the whole warp allocates the CTA's TMEM (one CTA per SM)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),

@@ -485,8 +485,8 @@ int h3q_gemm_swiglu_nvfp4(const uint8_t* a_codes, const uint8_t* a_scales, int64
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
-int h3q_gemm_error_flag(int* flag) {
-  static const char* fn = "h3q_gemm_error_flag";
+int h3q_kernel_error_flag(int* flag) {
+  static const char* fn = "h3q_kernel_error_flag";
   g_last_error.clear();
   if (flag == nullptr) return invalid(fn, "flag must not be NULL");
   cudaError_t err = h3q::gemm_error_flag(flag);

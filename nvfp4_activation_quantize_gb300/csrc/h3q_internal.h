@@ -90,8 +90,8 @@ cudaError_t launch_qkv_epilogue(const uint16_t* const x[3], const int64_t ld[3],
 cudaError_t launch_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, int64_t m, int64_t k, const uint8_t* b,
                                const uint8_t* sfb, int64_t n, const float* alpha, const float* gsf,
                                uint8_t* codes, uint8_t* scales, uint16_t* y, float* acc, cudaStream_t stream);
-// Reads and clears the flag a GEMM kernel sets when one of its bounded waits ran
-// out (synchronous).
+// Reads and clears the flag a kernel sets when one of its bounded waits ran out
+// (synchronous); the GEMM is the library's kernel with such waits.
 cudaError_t gemm_error_flag(int* flag);
 
 // RMSNorm + AdaLN -> NVFP4 on host buffers// RMSNorm + AdaLN -> NVFP4 on host buffers (x in, codes and scales out), the

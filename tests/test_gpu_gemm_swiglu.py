@@ -131,7 +131,7 @@ def test_ffn_up_65280x7168x37888(dev):
     worst, frac = _check_acc(acc.index_select(0, idx).cpu().numpy(), exact,
                              _abs_sum(a_codes[sample], a_sf[sample], b_codes, b_sf), k, "ffn-up sampled rows")
     print(f"accumulator: {frac:.4f} of sampled values exact, worst {worst:.3g} of the bound")
-    assert h3q.h3q_gemm_error_flag() == 0
+    assert h3q.h3q_kernel_error_flag() == 0
     step = 8192
     for r0 in range(0, m, step):
         r1 = min(m, r0 + step)
@@ -191,4 +191,4 @@ def test_outputs_stay_inside_their_buffers_and_repeat(dev):
         c2, s2 = h3q.h3q_gemm_swiglu_nvfp4(A, As, B, Bs, al, g, stream=s)
     torch.cuda.synchronize()
     assert torch.equal(c2, codes) and torch.equal(s2, scales)
-    assert h3q.h3q_gemm_error_flag() == 0
+    assert h3q.h3q_kernel_error_flag() == 0
