@@ -277,6 +277,104 @@ swiglu_ring_kernel(const uint16_t* __restrict__ gate, int64_t ld_gate, const uin
   ring_wait<0>();
 }
 
+// The producer with its loads staged through the per-warp cp.async ring (the
+// plain producer above), for the value-first packed projection with its
+// biases: gate and up get their per-column biases added (bf16(fl(x + b)), one
+// bf16x2 add per pair) after the ring.  Each warp keeps one 512-column segment
+// for all its rows -- warp w of the `active` = (warps / segs) * segs warps owns
+// segment w % segs and every (active / segs)-th row from w / segs -- so each
+// lane loads its 32 bytes of gate bias and of up bias once and holds them in
+// registers (re-reading them per row from L1 costs more than the ring gains:
+// the ring's shared memory leaves L1 too small for 2 x 2F bytes of bias).
+__global__ void __launch_bounds__(kRingThreads, 1)
+swiglu_ring_bias_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up, int64_t ld,
+                        int64_t rows, int64_t cols, const float* __restrict__ gsf_ptr,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                        const uint16_t* __restrict__ bias_gate, const uint16_t* __restrict__ bias_up) {
+  __shared__ float inv_table[128];
+  __shared__ __align__(16) float silu_table[2 * kTabHalf];
+  extern __shared__ __align__(16) uint8_t ring[];  // [warp][stage][gate, up][lane][32 bytes]
+  const float gsf = *gsf_ptr;
+  fill_inverse_scales(inv_table, gsf);
+  fill_silu_table(silu_table);
+  __syncthreads();
+  const char* table = reinterpret_cast<const char*>(silu_table);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t groups = cols >> 4;
+  const int64_t quads = cols >> 6;
+  const int64_t segs = (groups + 31) >> 5;
+  const int64_t prows = (rows + 127) >> 7 << 7;
+  const int64_t active = static_cast<int64_t>(gridDim.x) * kRingWarps / segs * segs;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * kRingWarps + warp;
+  if (w >= active) return;  // warp-uniform; no barrier follows
+  const int64_t seg = w % segs;
+  const int64_t row_step = active / segs;
+  const int64_t g = seg * 32 + lane;
+  const bool in_cols = g < groups;
+  const uint32_t sw = ((lane >> 2) & 1) * 16;
+  const uint32_t mine = static_cast<uint32_t>(__cvta_generic_to_shared(ring)) + warp * kRingWarpBytes + lane * 32;
+  Block16 bg, bu;
+  if (in_cols) {
+    load_reused(bias_gate + g * kBlock, bg);
+    load_reused(bias_up + g * kBlock, bu);
+  }
+  const uint16_t* gp = gate + g * kBlock;
+  const uint16_t* upp = up + g * kBlock;
+
+  int64_t crow = w / segs;  // the row computed
+  int64_t irow = crow;      // the next row copied
+  auto issue = [&](int stage) {
+    if (irow < rows && in_cols) {
+      const uint32_t d = mine + stage * 2048;
+      ring_cp16(d + sw, gp + irow * ld);
+      ring_cp16(d + (sw ^ 16), gp + irow * ld + 8);
+      ring_cp16(d + 1024 + sw, upp + irow * ld);
+      ring_cp16(d + 1024 + (sw ^ 16), upp + irow * ld + 8);
+    }
+    ring_commit();
+    irow += row_step;
+  };
+#pragma unroll
+  for (int s = 0; s < kRingStages - 1; ++s) issue(s);
+  int stage = 0;
+  while (crow < prows) {
+    ring_wait<kRingStages - 2>();  // this step's copies (this lane's) landed
+    const bool in_row = crow < rows;
+    Block16 gb, ub;
+    if (in_row && in_cols) {
+      const uint32_t d = mine + stage * 2048;
+      ring_ld16(d + sw, gb.w);
+      ring_ld16(d + (sw ^ 16), gb.w + 4);
+      ring_ld16(d + 1024 + sw, ub.w);
+      ring_ld16(d + 1024 + (sw ^ 16), ub.w + 4);
+      add_bias(gb, bg);
+      add_bias(ub, bu);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gb.w[i] = ub.w[i] = 0;
+    }
+    issue(stage == 0 ? kRingStages - 1 : stage - 1);
+    Block16 y;
+    uint32_t dw[8];
+    if (__all_sync(0xffffffffu, table_words(gb, dw))) {
+      swiglu_block_table(dw, ub, y, table);
+    } else if (__all_sync(0xffffffffu, block_amax(gb) <= kFastLimit)) {
+      swiglu_block<true>(gb, ub, y);
+    } else {
+      swiglu_block<false>(gb, ub, y);
+    }
+    Quantized q = quantize_block<true>(y, gsf, inv_table);
+    if (!in_row) q.sf = 0;
+    if (in_row && in_cols) store_codes(codes + crow * (cols >> 1) + g * 8, q.codes_lo, q.codes_hi);
+    store_scale_quad(scales, crow, g, quads, q.sf, in_cols);
+    stage = stage + 1 == kRingStages ? 0 : stage + 1;
+    crow += row_step;
+  }
+  ring_wait<0>();
+}
+
 }  // namespace
 
 cudaError_t launch_swiglu(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
@@ -301,12 +399,22 @@ cudaError_t launch_swiglu_packed(const uint16_t* o, int64_t ld_o, const uint16_t
   const int64_t segs = (f / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false, true>),
-                                      kThreads, 0, (work + kWarps - 1) / kWarps, &blocks);
+  const int smem = kRingWarps * kRingWarpBytes;
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_ring_bias_kernel), kRingThreads,
+                                      smem, (work + kRingWarps - 1) / kRingWarps, &blocks);
   if (err != cudaSuccess) return err;
-  // value first: up = o[:, :f] with bias[:f], gate = o[:, f:] with bias[f:]
-  swiglu_kernel<false, true><<<blocks, kThreads, 0, stream>>>(o + f, ld_o, o, ld_o, rows, f, gsf,
-                                                              codes, scales, nullptr, bias + f, bias);
+  if (int64_t{blocks} * kRingWarps >= segs) {
+    // value first: up = o[:, :f] with bias[:f], gate = o[:, f:] with bias[f:]
+    swiglu_ring_bias_kernel<<<blocks, kRingThreads, smem, stream>>>(o + f, o, ld_o, rows, f, gsf, codes, scales,
+                                                                    bias + f, bias);
+    return cudaGetLastError();
+  }
+  // rows wider than one segment per warp of the grid: warps cycle over segments
+  err = persistent_blocks(reinterpret_cast<const void*>(&swiglu_kernel<false, true>), kThreads, 0,
+                          (work + kWarps - 1) / kWarps, &blocks);
+  if (err != cudaSuccess) return err;
+  swiglu_kernel<false, true><<<blocks, kThreads, 0, stream>>>(o + f, ld_o, o, ld_o, rows, f, gsf, codes, scales,
+                                                              nullptr, bias + f, bias);
   return cudaGetLastError();
 }
 
