@@ -441,7 +441,82 @@ def run_ours(args, rank, world, dev):
     return result
 
 
+def _cpulist(text: str) -> list[int]:
+    """'0-3,8,10-11' -> [0, 1, 2, 3, 8, 10, 11]."""
+    cpus = []
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.extend(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_locality(dev) -> dict:
+    """The GPU's PCI address, its NUMA node and the CPUs local to it, from sysfs
+    (read only; {} where the files are missing)."""
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        bus = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    except AttributeError:
+        return {}
+    base = f"/sys/bus/pci/devices/{bus}"
+    out = {"pci": bus}
+    try:
+        with open(f"{base}/numa_node") as f:
+            out["numa_node"] = int(f.read().strip())
+        with open(f"{base}/local_cpulist") as f:
+            out["local_cpus"] = _cpulist(f.read())
+    except OSError:
+        pass
+    return out
+
+
+def pages_by_node(t: torch.Tensor) -> dict:
+    """How the pages of a host tensor's mapping are spread over NUMA nodes
+    (/proc/self/numa_maps: the mapping that contains its first byte)."""
+    addr = t.data_ptr()
+    try:
+        with open("/proc/self/maps") as f:
+            start = None
+            for line in f:
+                lo, hi = (int(v, 16) for v in line.split()[0].split("-"))
+                if lo <= addr < hi:
+                    start = lo
+                    break
+        if start is None:
+            return {}
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                fields = line.split()
+                if int(fields[0], 16) == start:
+                    return {k: int(v) for k, v in (x.split("=") for x in fields[2:])
+                            if k.startswith("N") and k[1:].isdigit()}
+    except (OSError, ValueError):
+        pass
+    return {}
+
+
 def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
+    """Runs measure_e2e_placed with this thread (the one that allocates the pinned
+    buffers and enqueues the copies) on the CPUs local to the GPU, so the pinned
+    pages land on the GPU's own node; the placement is recorded."""
+    loc = gpu_locality(dev)
+    before = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    cpus = [c for c in loc.get("local_cpus", []) if before is None or c in before]
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        out = measure_e2e_placed(h3q, dev, stream, w, gsf, args, world)
+    finally:
+        if cpus and before is not None:
+            os.sched_setaffinity(0, before)
+    out["placement"] = {"gpu": loc, "affinity": cpus or (sorted(before) if before else None),
+                        "x_pages_by_node": out.pop("_x_pages", {})}
+    return out
+
+
+def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
     """The same metric through the C-ABI host-buffer call (h3q_rmsnorm_adaln_nvfp4_host,
     through HostPipeline): each step copies gamma and the modulation table from pinned
     host memory to the device, then the call copies x in, runs the producer and copies
@@ -450,7 +525,8 @@ def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
     region (CUDA events on the caller's stream) covers every copy of the step."""
     from nvfp4_activation_quantize_gb300.host import HostPipeline
 
-    hx = w["x"].cpu().pin_memory()
+    hx = torch.empty(w["x"].shape, dtype=w["x"].dtype).pin_memory()
+    hx.copy_(w["x"])
     hg = w["gamma"].cpu().pin_memory()
     ht = w["table"].cpu().pin_memory()
     hc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8).pin_memory()
@@ -480,6 +556,7 @@ def measure_e2e(h3q, dev, stream, w, gsf, args, world=1):
         "call": "h3q_rmsnorm_adaln_nvfp4_host",
         "pipeline": {"chunk_rows": pipe.chunk_rows, "depth": pipe.depth, "streams": 3},
         "check": e2e_matches(h3q, dev, w, gsf, hc, hs),
+        "_x_pages": pages_by_node(hx),
     }
     if world == 1:
         link = host_link(dev)
