@@ -115,8 +115,9 @@ def fp4_peak():
 # The sources each kernel is compiled from (its own file and the shared device header).
 KERNEL_SOURCES = {
     "adaln_block_kernel": ("adaln.cu", "h3q_device.cuh"),
-    "swiglu_kernel": ("swiglu.cu", "h3q_device.cuh"),
-    "swiglu_ring_kernel": ("swiglu.cu", "h3q_device.cuh"),
+    "swiglu_kernel": ("swiglu.cu", "h3q_device.cuh", "h3q_silu.cuh"),
+    "swiglu_ring_kernel": ("swiglu.cu", "h3q_device.cuh", "h3q_silu.cuh"),
+    "gemm_swiglu_kernel": ("gemm_swiglu.cu", "h3q_device.cuh", "h3q_silu.cuh", "h3q_async.cuh"),
     "quantize_kernel": ("quantize.cu", "h3q_device.cuh"),
 }
 
