@@ -563,8 +563,31 @@ def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
         link = host_link(dev)
         bound = link_bound_ms(h2d, d2h, link)
         out["host_link"] = dict(link, bound_ms_per_step=round(bound, 3),
-                                frac_of_link_bound=round(bound / (total_ms / steps), 3))
+                                frac_of_link_bound=round(bound / (total_ms / steps), 3),
+                                step_buffers=buffer_rates(dev, hx, hc))
     return out
+
+
+def buffer_rates(dev, hx, hc, reps: int = 3) -> dict:
+    """Plain copy rates of the step's own pinned buffers (x in, codes out), beside
+    host_link's fresh buffers: a host buffer that copies slower than fresh pinned
+    memory on the same box points at its backing, not at the pipeline."""
+    dx = torch.empty(hx.shape, dtype=hx.dtype, device=dev)
+    dc = torch.empty(hc.shape, dtype=hc.dtype, device=dev)
+
+    def rate(fn, nbytes):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return round(reps * nbytes / (time.perf_counter() - t0) / 1e9, 1)
+
+    res = {"x_h2d_gbs": rate(lambda: dx.copy_(hx, non_blocking=True), hx.numel() * hx.element_size()),
+           "codes_d2h_gbs": rate(lambda: hc.copy_(dc, non_blocking=True), hc.numel())}
+    del dx, dc
+    return res
 
 
 def host_link(dev, nbytes: int = 512 << 20, reps: int = 8) -> dict:
