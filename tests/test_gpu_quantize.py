@@ -142,12 +142,15 @@ def test_dequantize_matches_oracle(dev):
 
 
 def test_dequantize_random_codes_every_scale(dev):
+    """Random codes under every scale code; global scales that keep every value
+    normal and ones that push the small scales' values below the normal range
+    (2^120: subnormal and zero results) or the large ones' past it (2^-118: inf)."""
     rng = np.random.default_rng(14)
     rows, cols = 129, 640
     codes = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
     sf = rng.integers(0, 0x7F, (rows, cols // 16), dtype=np.uint8)
     scales = oracle.swizzle_scales(sf, rows, cols)
-    for gsf in (1.0, 0.001, 123.5):
+    for gsf in (1.0, 0.001, 123.5, 2.0**120, 2.0**-118):
         out = h3q.h3q_dequantize_nvfp4(torch.from_numpy(codes).to(dev),
                                        torch.from_numpy(scales.reshape(-1, cols // 16)).to(dev),
                                        gsf_tensor(gsf, dev))
