@@ -764,28 +764,33 @@ def measure_producers(h3q, dev, stream, args):
     c = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
     s = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8, device=dev)
 
+    rstd = torch.empty(ROWS, dtype=torch.float32, device=dev)
+
     def dynamic_step():
+        # the abs-max pass hands each row's rstd to the second pass, which then
+        # forms no statistics of its own
         amax.zero_()
         h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], rows_per_frame=RPF, eps=w["eps"],
-                                   amax=amax, stream=stream)
+                                   amax=amax, row_rstd=rstd, stream=stream)
         h3q.h3q_global_scale_from_amax(amax, g, stream=stream)
-        h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], g, rows_per_frame=RPF,
-                                    eps=w["eps"], codes=c, scales=s, stream=stream)
+        h3q.h3q_rmsnorm_adaln_nvfp4_from_rstd(w["x"], w["gamma"], w["table"], rstd, g, rows_per_frame=RPF,
+                                              codes=c, scales=s, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
             dynamic_step()
     _, per = time_launches(dynamic_step, n, stream)
     res["adaln_dynamic_scale_65280x7168"] = entry(adaln_bytes(ROWS, COLS, FRAMES), per, ROWS)
-    res["adaln_dynamic_scale_65280x7168"]["note"] = ("abs-max pass + device scale + producer; x is read "
-                                                     "twice, GB/s by the single-pass bytes")
+    res["adaln_dynamic_scale_65280x7168"]["note"] = ("abs-max pass (writing each row's rstd) + device scale + "
+                                                     "producer taking the rstd; x is read twice, GB/s by the "
+                                                     "single-pass bytes")
     # the least a per-call abs-max scale can move: x read by both passes (the whole
     # tensor's maximum is needed before any row is quantized), the outputs once
-    two_pass = adaln_bytes(ROWS, COLS, FRAMES) + 2 * ROWS * COLS + 2 * COLS + FRAMES * 2 * COLS * 2
+    two_pass = adaln_bytes(ROWS, COLS, FRAMES) + 2 * ROWS * COLS + 2 * COLS + FRAMES * 2 * COLS * 2 + 2 * 4 * ROWS
     dyn = res["adaln_dynamic_scale_65280x7168"]
     dyn["two_pass_algorithmic_bytes"] = two_pass
     dyn["frac_of_peak_two_pass"] = round(two_pass / (dyn["median_launch_ms"] * 1e-3) / 1e9 / peak, 4)
-    del w, c, s
+    del w, c, s, rstd
 
     # residual fold + RMSNorm + AdaLN: h (fp32) is read and written back each launch
     torch.cuda.empty_cache()

@@ -87,7 +87,7 @@ extern "C" {
 #define H3Q_ERR_INVALID_ARGUMENT 1
 #define H3Q_ERR_CUDA 2
 
-#define H3Q_ABI_VERSION 3
+#define H3Q_ABI_VERSION 4
 
 /* Rows of the scale matrix: rows rounded up to a multiple of 128. */
 static inline int64_t h3q_padded_rows(int64_t rows) { return (rows + 127) / 128 * 128; }
@@ -278,6 +278,11 @@ int h3q_residual_rmsnorm_adaln_nvfp4(float *h, int64_t ld_h, const void *o, int6
  *
  * Preconditions and status codes are those of the matching producer (shapes,
  * alignment, ld, frames), plus: amax not NULL and not overlapping an input.
+ *
+ * h3q_rmsnorm_adaln_amax also writes each row's rstd to row_rstd when it is not
+ * NULL (fp32 [rows], 4-byte aligned, overlapping neither an input nor amax): the
+ * pass forms the row statistics anyway, in the producer's canonical order, so
+ * h3q_rmsnorm_adaln_nvfp4_from_rstd can then quantize without forming them again.
  */
 int h3q_amax_bf16(const void *x, int64_t ld_x, int64_t rows, int64_t cols, float *amax,
                   void *stream);
@@ -285,7 +290,24 @@ int h3q_amax_bf16(const void *x, int64_t ld_x, int64_t rows, int64_t cols, float
 int h3q_rmsnorm_adaln_amax(const void *x, int64_t ld_x, const void *gamma,
                            const void *mod_table, int64_t num_frames, const int32_t *row_frame,
                            int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
-                           float *amax, void *stream);
+                           float *amax, float *row_rstd, void *stream);
+
+/*
+ * The RMSNorm + AdaLN producer with each row's rstd given: the second pass of a
+ * dynamic scale, after h3q_rmsnorm_adaln_amax wrote row_rstd.  y and its NVFP4 are
+ * those of h3q_rmsnorm_adaln_nvfp4 with rstd = row_rstd[r] in place of the row's
+ * own statistics (so, with the abs-max pass's row_rstd, byte for byte the same
+ * output); eps has no role.  Arguments as h3q_rmsnorm_adaln_nvfp4, plus:
+ *
+ *   row_rstd  fp32 [rows] on the device, 4-byte aligned, not NULL, overlapping no
+ *             output.
+ */
+int h3q_rmsnorm_adaln_nvfp4_from_rstd(const void *x, int64_t ld_x, const void *gamma,
+                                      const void *mod_table, int64_t num_frames,
+                                      const int32_t *row_frame, int64_t rows_per_frame,
+                                      const float *row_rstd, int64_t rows, int64_t cols,
+                                      const float *global_scale, uint8_t *codes, uint8_t *scales,
+                                      void *stream);
 
 int h3q_swiglu_amax(const void *gate, int64_t ld_gate, const void *up, int64_t ld_up,
                     int64_t rows, int64_t cols, float *amax, void *stream);

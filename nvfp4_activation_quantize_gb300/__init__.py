@@ -22,7 +22,8 @@ __all__ = [
     "H3Q_OK", "H3Q_ERR_INVALID_ARGUMENT", "H3Q_ERR_CUDA", "H3QError", "library", "library_path",
     "padded_rows", "scale_bytes", "h3q_quantize_nvfp4", "h3q_rmsnorm_adaln_nvfp4",
     "h3q_swiglu_nvfp4", "h3q_dequantize_nvfp4", "h3q_last_error", "h3q_abi_version",
-    "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_swiglu_amax", "h3q_global_scale_from_amax",
+    "h3q_amax_bf16", "h3q_rmsnorm_adaln_amax", "h3q_rmsnorm_adaln_nvfp4_from_rstd", "h3q_swiglu_amax",
+    "h3q_global_scale_from_amax",
     "h3q_quantize_nvfp4_dynamic", "h3q_residual_rmsnorm_adaln_nvfp4", "h3q_swiglu_packed_nvfp4",
     "h3q_qkv_epilogue", "h3q_rmsnorm_adaln_nvfp4_host", "host_workspace_bytes",
     "h3q_gemm_swiglu_nvfp4", "h3q_kernel_error_flag",
@@ -41,7 +42,8 @@ _SIGNATURES = {
     "h3q_swiglu_nvfp4": [_P, _I64, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "h3q_dequantize_nvfp4": [_P, _P, _I64, _I64, _P, _P, _P],
     "h3q_amax_bf16": [_P, _I64, _I64, _I64, _P, _P],
-    "h3q_rmsnorm_adaln_amax": [_P, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _I64, _I64, _P, _P],
+    "h3q_rmsnorm_adaln_amax": [_P, _I64, _P, _P, _I64, _P, _I64, ctypes.c_float, _I64, _I64, _P, _P, _P],
+    "h3q_rmsnorm_adaln_nvfp4_from_rstd": [_P, _I64, _P, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P],
     "h3q_swiglu_amax": [_P, _I64, _P, _I64, _I64, _I64, _P, _P],
     "h3q_global_scale_from_amax": [_P, _P, _P],
     "h3q_quantize_nvfp4_dynamic": [_P, _I64, _I64, _I64, _P, _P, _P, _P],
@@ -309,9 +311,10 @@ def h3q_amax_bf16(x, amax=None, stream=None):
 
 
 def h3q_rmsnorm_adaln_amax(x, gamma, mod_table, *, row_frame=None, rows_per_frame=None, eps=1e-6,
-                           amax=None, stream=None):
+                           amax=None, row_rstd=None, stream=None):
     """Fold max |y| of the RMSNorm + AdaLN output y (the bf16 values the producer
-    quantizes, same arguments) into ``amax``; returns amax."""
+    quantizes, same arguments) into ``amax``; returns amax.  ``row_rstd`` (fp32
+    [rows], optional) receives each row's rstd, for h3q_rmsnorm_adaln_nvfp4_from_rstd."""
     import torch
 
     x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
@@ -328,12 +331,48 @@ def h3q_rmsnorm_adaln_amax(x, gamma, mod_table, *, row_frame=None, rows_per_fram
     elif rows_per_frame is None:
         raise ValueError("give row_frame or rows_per_frame")
     amax = _amax_buffer(amax, dev)
+    rstd_ptr = None
+    if row_rstd is not None:
+        _contiguous("row_rstd", row_rstd, torch.float32, (rows,), dev)
+        rstd_ptr = row_rstd.data_ptr()
     with torch.cuda.device(dev):
         rc = library().h3q_rmsnorm_adaln_amax(
             x.data_ptr(), ld, gamma.data_ptr(), mod_table.data_ptr(), mod_table.shape[0], rf_ptr,
-            int(rows_per_frame), float(eps), rows, cols, amax.data_ptr(), _stream(stream, dev))
+            int(rows_per_frame), float(eps), rows, cols, amax.data_ptr(), rstd_ptr, _stream(stream, dev))
     _check("h3q_rmsnorm_adaln_amax", rc)
     return amax
+
+
+def h3q_rmsnorm_adaln_nvfp4_from_rstd(x, gamma, mod_table, row_rstd, global_scale, *, row_frame=None,
+                                      rows_per_frame=None, codes=None, scales=None, stream=None):
+    """The RMSNorm + AdaLN producer with each row's rstd given (fp32 [rows], e.g. the
+    abs-max pass's ``row_rstd``): the statistics are not formed again.  Returns
+    (codes, scales)."""
+    import torch
+
+    x, rows, cols, ld = _rows_view("x", x, torch.bfloat16)
+    dev = x.device
+    _contiguous("gamma", gamma, torch.bfloat16, (cols,), dev)
+    _cuda_tensor("mod_table", mod_table, torch.bfloat16, dev)
+    if mod_table.dim() != 3 or mod_table.shape[1:] != (2, cols) or not mod_table.is_contiguous():
+        raise ValueError("mod_table must be contiguous [frames, 2, cols]")
+    _contiguous("row_rstd", row_rstd, torch.float32, (rows,), dev)
+    rf_ptr = None
+    if row_frame is not None:
+        _contiguous("row_frame", row_frame, torch.int32, (rows,), dev)
+        rf_ptr = row_frame.data_ptr()
+        rows_per_frame = 0
+    elif rows_per_frame is None:
+        raise ValueError("give row_frame or rows_per_frame")
+    codes, scales = _outputs(dev, rows, cols, codes, scales)
+    gsf = _gsf(global_scale, dev)
+    with torch.cuda.device(dev):
+        rc = library().h3q_rmsnorm_adaln_nvfp4_from_rstd(
+            x.data_ptr(), ld, gamma.data_ptr(), mod_table.data_ptr(), mod_table.shape[0], rf_ptr,
+            int(rows_per_frame), row_rstd.data_ptr(), rows, cols, gsf.data_ptr(), codes.data_ptr(),
+            scales.data_ptr(), _stream(stream, dev))
+    _check("h3q_rmsnorm_adaln_nvfp4_from_rstd", rc)
+    return codes, scales
 
 
 def h3q_swiglu_amax(gate, up, amax=None, stream=None):

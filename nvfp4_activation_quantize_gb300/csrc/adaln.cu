@@ -58,6 +58,7 @@ struct AdalnArgs {
   uint8_t* scales;
   float* row_rstd;
   float* amax;  // abs-max pass: fold max |y| into *amax instead of quantizing (codes, scales unused)
+  const float* rstd_in;  // each row's rstd given (from an abs-max pass): the statistics are not formed
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
@@ -336,6 +337,11 @@ __global__ void __launch_bounds__(NT, 2) adaln_kernel(const AdalnArgs a) {
     gather_totals<2>(totals, static_cast<int>(p & 1), ss);
     rstd[0] = rstd_of(ss[0], cols_f, a.eps);
     rstd[1] = rstd_of(ss[1], cols_f, a.eps);
+    if (a.rstd_in != nullptr) {  // the rows' rstd given
+      const int64_t r = r_begin + 2 * p;
+      rstd[0] = a.rstd_in[r];
+      rstd[1] = r + 1 < r_end ? a.rstd_in[r + 1] : 0.0f;
+    }
   };
 
   float rstd[2] = {0.0f, 0.0f};
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) adaln_generic_kernel(const AdalnArgs
     for (int64_t c = t; c < chunks; c += kThreads) accumulate(load16_stream(xr + c * 8), acc[0]);
     float ss[1];
     row_sums<1>(acc, totals, static_cast<int>(r & 1), ss);
-    const float rstd[1] = {rstd_of(ss[0], static_cast<float>(a.cols), a.eps)};
+    const float rstd[1] = {a.rstd_in != nullptr ? a.rstd_in[r] : rstd_of(ss[0], static_cast<float>(a.cols), a.eps)};
     if (a.row_rstd != nullptr && t == 0) a.row_rstd[r] = rstd[0];
     for (int64_t c0 = 0; c0 < chunks; c0 += kThreads) {  // CTA-uniform trip count
       const int64_t c = c0 + t;
@@ -571,7 +577,7 @@ struct RowInfo {
   int64_t scale_off;  // byte offset of the row's part of a scale word (scale_row_offset)
 };
 
-template <int NB, int C1, bool AMAX>
+template <int NB, int C1, bool AMAX, bool GIVEN = false>
 __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   constexpr int R = NB / kLanes128;
   constexpr int kStages = kBlockStages;
@@ -630,7 +636,7 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
     ++issued;
   };
   auto pass1 = [&](int q, int stage) {
-    if (q >= steps || !p1) return;
+    if (GIVEN || q >= steps || !p1) return;  // GIVEN: the rows' rstd are given, no sums
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -645,14 +651,26 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
     for (int o = 16; o >= 1; o >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, o));
     if (lane == 0) totals[q & 1][grp][ppi & 3] = tot;
   };
-  // the stats warp: lane k < R publishes row k of step q
+  // the stats warp: lane k < R publishes row k of step q.  GIVEN: the rstd is read
+  // a step ahead of its publication, so the load is off the publishing chain.
   FrameCursor lane_cursor(a, r_begin + (lane < R ? lane : 0));
+  float given = 0.0f;
+  auto fetch_given = [&](int q) {
+    const int64_t r = r_begin + R * int64_t{q} + lane;
+    if (GIVEN && q < steps && lane < R && r < r_end) given = a.rstd_in[r];
+  };
+  fetch_given(0);
   auto stats = [&](int q) {
     if (q >= steps || lane >= R) return;
     const int64_t r = r_begin + R * int64_t{q} + lane;
     const float* T = totals[q & 1][lane];
     RowInfo info;
-    info.rstd = rstd_of(__fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3])), cols_f, a.eps);
+    if (GIVEN) {
+      info.rstd = given;
+      fetch_given(q + 1);
+    } else {
+      info.rstd = rstd_of(__fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3])), cols_f, a.eps);
+    }
     info.frame = r < r_end ? static_cast<int32_t>(lane_cursor.at(a, r)) : -1;
     info.scale_off = scale_row_offset(r, quads);
     rows_s[q & 1][lane] = info;
@@ -751,15 +769,15 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
     zero_padding_rows(a);
 }
 
-template <bool AMAX>
+template <bool AMAX, bool GIVEN>
 cudaError_t launch_block7168(const AdalnArgs& a, cudaStream_t stream) {
   constexpr int NB = 448, C1 = 7, R = NB / kLanes128;
   const int smem = kBlockStages * R * kLanes128 * C1 * 16;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1, AMAX>),
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&adaln_block_kernel<NB, C1, AMAX, GIVEN>),
                                       NB, smem, a.rows > 0 ? (a.rows + R - 1) / R : 1, &blocks);
   if (err != cudaSuccess) return err;
-  adaln_block_kernel<NB, C1, AMAX><<<blocks, NB, smem, stream>>>(a);
+  adaln_block_kernel<NB, C1, AMAX, GIVEN><<<blocks, NB, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -798,7 +816,9 @@ cudaError_t dispatch(const AdalnArgs& a, cudaStream_t stream) {
   if (per_lane <= 1) return launch_resident<128, 1, 1, 4, AMAX>(a, stream);
   if (per_lane <= 2) return launch_resident<128, 2, 2, 4, AMAX>(a, stream);
   if (per_lane <= 4) return launch_resident<128, 4, 4, 4, AMAX>(a, stream);
-  if (chunks == 2 * 448) return launch_block7168<AMAX>(a, stream);  // 7,168 columns
+  if (chunks == 2 * 448)  // 7,168 columns
+    return a.rstd_in != nullptr && !AMAX ? launch_block7168<false, true>(a, stream)
+                                         : launch_block7168<AMAX, false>(a, stream);
   if (per_lane <= 7) return launch_resident<128, 7, 7, 4, AMAX>(a, stream);
   if (per_lane <= 8) return launch_resident<128, 8, 8, 3, AMAX>(a, stream);
   return launch_generic<AMAX>(a, stream);
@@ -812,16 +832,25 @@ cudaError_t launch_adaln(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                          const float* gsf, uint8_t* codes, uint8_t* scales, float* row_rstd,
                          cudaStream_t stream) {
   const AdalnArgs a{x,    ld,   gamma, table,  num_frames, row_frame, rows_per_frame, eps,
-                    rows, cols, gsf,   codes,  scales,     row_rstd,  nullptr};
+                    rows, cols, gsf,   codes,  scales,     row_rstd,  nullptr, nullptr};
+  return dispatch<false>(a, stream);
+}
+
+cudaError_t launch_adaln_from_rstd(const uint16_t* x, int64_t ld, const uint16_t* gamma, const uint16_t* table,
+                                   int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
+                                   const float* rstd, int64_t rows, int64_t cols, const float* gsf,
+                                   uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const AdalnArgs a{x,    ld,   gamma, table,  num_frames, row_frame, rows_per_frame, 0.0f,
+                    rows, cols, gsf,   codes,  scales,     nullptr,   nullptr,        rstd};
   return dispatch<false>(a, stream);
 }
 
 cudaError_t launch_adaln_amax(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                               const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
                               int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
-                              float* amax, cudaStream_t stream) {
+                              float* amax, float* row_rstd, cudaStream_t stream) {
   const AdalnArgs a{x,    ld,   gamma,   table,   num_frames, row_frame, rows_per_frame, eps,
-                    rows, cols, nullptr, nullptr, nullptr,    nullptr,   amax};
+                    rows, cols, nullptr, nullptr, nullptr,    row_rstd,  amax,           nullptr};
   return dispatch<true>(a, stream);
 }
 

@@ -253,6 +253,44 @@ int h3q_rmsnorm_adaln_nvfp4(const void* x, int64_t ld_x, const void* gamma, cons
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 
+int h3q_rmsnorm_adaln_nvfp4_from_rstd(const void* x, int64_t ld_x, const void* gamma, const void* mod_table,
+                                      int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
+                                      const float* row_rstd, int64_t rows, int64_t cols,
+                                      const float* global_scale, uint8_t* codes, uint8_t* scales, void* stream) {
+  static const char* fn = "h3q_rmsnorm_adaln_nvfp4_from_rstd";
+  g_last_error.clear();
+  if (int e = check_shape(fn, rows, cols)) return e;
+  if (num_frames < 1) return invalid(fn, "num_frames must be >= 1");
+  if (num_frames > (int64_t(1) << 31)) return invalid(fn, "num_frames exceeds 2^31");
+  if (rows == 0) return H3Q_OK;
+  if (int e = check_input(fn, "x", x, ld_x, rows, cols)) return e;
+  if (int e = check_input(fn, "gamma", gamma, cols, 1, cols)) return e;
+  if (int e = check_input(fn, "mod_table", mod_table, cols, 2 * num_frames, cols)) return e;
+  if (int e = check_outputs(fn, codes, scales, global_scale)) return e;
+  if (row_frame != nullptr) {
+    if (!aligned(row_frame, 4)) return invalid(fn, "row_frame must be 4-byte aligned");
+  } else {
+    if (rows_per_frame < 1) return invalid(fn, "rows_per_frame must be >= 1 when row_frame is NULL");
+    if ((rows - 1) / rows_per_frame >= num_frames)
+      return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
+  }
+  if (row_rstd == nullptr) return invalid(fn, "row_rstd is NULL");
+  if (!aligned(row_rstd, 4)) return invalid(fn, "row_rstd must be 4-byte aligned");
+  const Span c = span(codes, h3q_code_bytes(rows, cols));
+  const Span s = span(scales, h3q_scale_bytes(rows, cols));
+  const Span ins[5] = {span(x, view_bytes(rows, cols, ld_x)), span(gamma, cols * 2),
+                       span(mod_table, num_frames * 4 * cols),
+                       row_frame ? span(row_frame, rows * 4) : Span{0, 0}, span(row_rstd, rows * 4)};
+  if (overlap(c, s)) return invalid(fn, "codes and scales overlap");
+  for (const Span& in : ins)
+    if (overlap(in, c) || overlap(in, s)) return invalid(fn, "an output overlaps an input");
+  cudaError_t err = h3q::launch_adaln_from_rstd(
+      static_cast<const uint16_t*>(x), ld_x, static_cast<const uint16_t*>(gamma),
+      static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, row_rstd, rows, cols,
+      global_scale, codes, scales, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
+}
+
 int h3q_swiglu_nvfp4(const void* gate, int64_t ld_gate, const void* up, int64_t ld_up,
                      int64_t rows, int64_t cols, const float* global_scale, uint8_t* codes,
                      uint8_t* scales, void* stream) {
@@ -357,7 +395,8 @@ int h3q_amax_bf16(const void* x, int64_t ld_x, int64_t rows, int64_t cols, float
 
 int h3q_rmsnorm_adaln_amax(const void* x, int64_t ld_x, const void* gamma, const void* mod_table,
                            int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
-                           float eps, int64_t rows, int64_t cols, float* amax, void* stream) {
+                           float eps, int64_t rows, int64_t cols, float* amax, float* row_rstd,
+                           void* stream) {
   static const char* fn = "h3q_rmsnorm_adaln_amax";
   g_last_error.clear();
   if (int e = check_shape(fn, rows, cols)) return e;
@@ -377,14 +416,22 @@ int h3q_rmsnorm_adaln_amax(const void* x, int64_t ld_x, const void* gamma, const
       return invalid(fn, "rows / rows_per_frame reaches past the modulation table");
   }
   const Span am = span(amax, 4);
-  if (overlap(am, span(x, view_bytes(rows, cols, ld_x))) || overlap(am, span(gamma, cols * 2)) ||
-      overlap(am, span(mod_table, num_frames * 4 * cols)) ||
-      (row_frame != nullptr && overlap(am, span(row_frame, rows * 4))))
-    return invalid(fn, "amax overlaps an input");
+  const Span ins[4] = {span(x, view_bytes(rows, cols, ld_x)), span(gamma, cols * 2),
+                       span(mod_table, num_frames * 4 * cols),
+                       row_frame ? span(row_frame, rows * 4) : Span{0, 0}};
+  for (const Span& in : ins)
+    if (overlap(am, in)) return invalid(fn, "amax overlaps an input");
+  if (row_rstd != nullptr) {
+    if (!aligned(row_rstd, 4)) return invalid(fn, "row_rstd must be 4-byte aligned");
+    const Span r = span(row_rstd, rows * 4);
+    if (overlap(r, am)) return invalid(fn, "row_rstd overlaps amax");
+    for (const Span& in : ins)
+      if (overlap(r, in)) return invalid(fn, "row_rstd overlaps an input");
+  }
   cudaError_t err = h3q::launch_adaln_amax(
       static_cast<const uint16_t*>(x), ld_x, static_cast<const uint16_t*>(gamma),
       static_cast<const uint16_t*>(mod_table), num_frames, row_frame, rows_per_frame, eps, rows,
-      cols, amax, static_cast<cudaStream_t>(stream));
+      cols, amax, row_rstd, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 

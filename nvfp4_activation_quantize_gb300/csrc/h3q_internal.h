@@ -41,7 +41,12 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t ld, int64_t rows, int64_
 cudaError_t launch_adaln_amax(const uint16_t* x, int64_t ld, const uint16_t* gamma,
                               const uint16_t* table, int64_t num_frames, const int32_t* row_frame,
                               int64_t rows_per_frame, float eps, int64_t rows, int64_t cols,
-                              float* amax, cudaStream_t stream);
+                              float* amax, float* row_rstd, cudaStream_t stream);
+// The AdaLN producer with each row's rstd given (an abs-max pass's row_rstd).
+cudaError_t launch_adaln_from_rstd(const uint16_t* x, int64_t ld, const uint16_t* gamma, const uint16_t* table,
+                                   int64_t num_frames, const int32_t* row_frame, int64_t rows_per_frame,
+                                   const float* rstd, int64_t rows, int64_t cols, const float* gsf,
+                                   uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 cudaError_t launch_swiglu_amax(const uint16_t* gate, int64_t ld_gate, const uint16_t* up,
                                int64_t ld_up, int64_t rows, int64_t cols, float* amax,
                                cudaStream_t stream);

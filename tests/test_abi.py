@@ -37,7 +37,7 @@ def test_header_declares_the_four_calls():
 def test_every_declared_symbol_is_exported(lib):
     for fn in _declared_functions():
         assert hasattr(lib, fn), f"{fn} is declared in h3q.h but not exported"
-    assert lib.h3q_abi_version() == 3
+    assert lib.h3q_abi_version() == 4
 
 
 def _q(lib, x=0x10000, ld=256, rows=4, cols=256, gsf=0x20000, codes=0x30000, scales=0x40000):
@@ -123,8 +123,9 @@ def test_dynamic_scale_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.h3q_amax_bf16(0x100000, 256, 4, 256, 0x100010, None) == 1  # inside x
     assert lib.h3q_amax_bf16(0x100000, 256, 4, 100, 0x200000, None) == 1
     assert lib.h3q_amax_bf16(None, 256, 0, 256, None, None) == h3q.H3Q_OK  # no rows: no-op
-    # h3q_rmsnorm_adaln_amax(x, ld, gamma, table, frames, row_frame, rpf, eps, rows, cols, amax, stream)
-    args = [0x100000, 256, 0x200000, 0x300000, 4, None, 16, 1e-6, 64, 256, 0x400000, None]
+    # h3q_rmsnorm_adaln_amax(x, ld, gamma, table, frames, row_frame, rpf, eps, rows, cols, amax,
+    #                        row_rstd, stream)
+    args = [0x100000, 256, 0x200000, 0x300000, 4, None, 16, 1e-6, 64, 256, 0x400000, None, None]
     bad = list(args); bad[6] = 15
     assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "modulation table" in h3q.h3q_last_error()
     bad = list(args); bad[10] = None
@@ -133,6 +134,12 @@ def test_dynamic_scale_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "overlaps" in h3q.h3q_last_error()
     bad = list(args); bad[7] = -1.0
     assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1
+    bad = list(args); bad[11] = 0x500002  # row_rstd misaligned
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "row_rstd" in h3q.h3q_last_error()
+    bad = list(args); bad[11] = 0x400000  # row_rstd on amax
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "overlaps" in h3q.h3q_last_error()
+    bad = list(args); bad[11] = 0x100100  # row_rstd inside x
+    assert lib.h3q_rmsnorm_adaln_amax(*bad) == 1 and "overlaps" in h3q.h3q_last_error()
     # h3q_swiglu_amax(gate, ldg, up, ldu, rows, cols, amax, stream)
     assert lib.h3q_swiglu_amax(0x100000, 256, None, 256, 8, 256, 0x400000, None) == 1
     assert lib.h3q_swiglu_amax(0x100000, 256, 0x200000, 256, 8, 256, 0x200100, None) == 1
@@ -274,3 +281,24 @@ def test_gemm_swiglu_host_checks_run_before_any_cuda_call():
     assert "overlap" in h3q.h3q_last_error()
     assert f(A, AS, 4, 256, B, BS, 256, AL, G, A, S, None, None, None) == 1       # codes over a
     assert f(None, None, 0, 256, None, None, 256, None, None, None, None, None, None, None) == 0  # m = 0
+
+
+def test_from_rstd_producer_rejects_bad_arguments_on_the_host(lib):
+    # h3q_rmsnorm_adaln_nvfp4_from_rstd(x, ld, gamma, table, frames, row_frame, rpf, row_rstd, rows, cols,
+    #                                   gsf, codes, scales, stream)
+    args = [0x100000, 256, 0x200000, 0x300000, 4, None, 16, 0x500000, 64, 256, 0x600000, 0x700000,
+            0x800000, None]
+    bad = list(args); bad[7] = None
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1 and "row_rstd" in h3q.h3q_last_error()
+    bad = list(args); bad[7] = 0x500002
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1 and "aligned" in h3q.h3q_last_error()
+    bad = list(args); bad[7] = 0x700010  # row_rstd inside the codes
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1 and "overlaps" in h3q.h3q_last_error()
+    bad = list(args); bad[6] = 15
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1 and "modulation table" in h3q.h3q_last_error()
+    bad = list(args); bad[9] = 100
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1
+    bad = list(args); bad[0] = None
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == 1
+    bad = list(args); bad[8] = 0
+    assert lib.h3q_rmsnorm_adaln_nvfp4_from_rstd(*bad) == h3q.H3Q_OK  # no rows: no-op

@@ -140,14 +140,21 @@ def test_dynamic_swiglu_chain(dev):
 
 def test_dynamic_adaln_65280x7168_every_row(dev):
     """The 65,280 x 7,168 AdaLN workload with a per-call abs-max instead of the
-    calibrated static scale: the abs-max, the scale and every byte of the outputs."""
+    calibrated static scale: the abs-max, the scale, every row's rstd handed from
+    the abs-max pass to the second pass, and every byte of the outputs of both
+    second passes (the producer forming its own statistics, and the one taking the
+    abs-max pass's rstd)."""
     w = workloads.adaln_inputs(dev)
     rows, cols = w["x"].shape
     rpf = w["rows_per_frame"]
-    amax = h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], rows_per_frame=rpf, eps=w["eps"])
+    rstd = torch.empty(rows, dtype=torch.float32, device=dev)
+    amax = h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], rows_per_frame=rpf, eps=w["eps"],
+                                      row_rstd=rstd)
     gsf = h3q.h3q_global_scale_from_amax(amax)
     codes, scales = h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], gsf, rows_per_frame=rpf,
                                                 eps=w["eps"])
+    codes2, scales2 = h3q.h3q_rmsnorm_adaln_nvfp4_from_rstd(w["x"], w["gamma"], w["table"], rstd, gsf,
+                                                            rows_per_frame=rpf)
     frames = np.arange(rows) // rpf
     _, _, _, y = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
                                    None, want_y=True, threads=THREADS)
@@ -155,6 +162,42 @@ def test_dynamic_adaln_65280x7168_every_row(dev):
     _eq(amax, a, "full-size amax")
     g = oracle.global_scale_from_amax(a)
     _eq(gsf, g, "full-size gsf")
-    co, so, _, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
-                                     g, threads=THREADS)
+    co, so, rstd_o, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                          g, threads=THREADS)
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), rstd_o.view(np.uint32)), "abs-max pass rstd"
     check_full(codes, scales, rows, cols, co, so, "dynamic adaln 65280x7168")
+    check_full(codes2, scales2, rows, cols, co, so, "dynamic adaln from rstd 65280x7168")
+
+
+@pytest.mark.parametrize("rows,cols,use_row_frame", [(5, 64, False), (130, 256, True), (257, 1024, False),
+                                                     (100, 2048, True), (1, 7168, False), (4, 7168, True),
+                                                     (457, 7168, False), (458, 7168, True), (64, 8192, False),
+                                                     (40, 16384, True), (33, 1088, False)])
+def test_adaln_from_rstd_every_route(dev, rows, cols, use_row_frame):
+    """The abs-max pass's row_rstd equals the oracle's rstd bit for bit, and the
+    producer given it writes the oracle's codes and scales, on every kernel route
+    (resident kernels, the 7,168-column block kernel with its short last steps, the
+    generic one), with rows_per_frame and with a row -> frame array."""
+    frames_n = 5
+    rpf = max(1, (rows + frames_n - 1) // frames_n)
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=frames_n, rows_per_frame=rpf,
+                               seed=rows * 3 + cols)
+    if use_row_frame:
+        rf = torch.randint(0, frames_n, (rows,), generator=torch.Generator().manual_seed(rows), dtype=torch.int32)
+        frames = rf.numpy()
+        kw = {"row_frame": rf.to(dev)}
+    else:
+        frames = np.arange(rows) // rpf
+        kw = {"rows_per_frame": rpf}
+    rstd = torch.empty(rows, dtype=torch.float32, device=dev)
+    amax = h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], eps=w["eps"], row_rstd=rstd, **kw)
+    gsf = h3q.h3q_global_scale_from_amax(amax)
+    codes, scales = h3q.h3q_rmsnorm_adaln_nvfp4_from_rstd(w["x"], w["gamma"], w["table"], rstd, gsf, **kw)
+    _, _, _, y = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                   None, want_y=True, threads=THREADS)
+    g = oracle.global_scale_from_amax(oracle.amax_bf16(y))
+    _eq(gsf, g, f"gsf {rows}x{cols}")
+    co, so, rstd_o, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                          g, threads=THREADS)
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), rstd_o.view(np.uint32)), f"rstd {rows}x{cols}"
+    check_full(codes, scales, rows, cols, co, so, f"adaln from rstd {rows}x{cols}")
