@@ -321,10 +321,11 @@ int h3q_global_scale_from_amax(const float *amax, float *global_scale, void *str
  * abs-max pass over x whose CTAs write their partial maxima into a fixed
  * device array inside the library (a file-scope __device__ array of 4,096
  * floats, one per CUDA context, its address looked up in the current context
- * on every call: a lookup, not an allocation), reduces them
- * into *global_scale = fl(2688 / max |x|) (0 -> 1, +inf clamped), and then
- * quantizes x as h3q_quantize_nvfp4 does with that scale.  Outputs: codes,
- * scales and the global scale used (a device fp32 scalar written here).
+ * on every call: a lookup, not an allocation); then the quantize, launched as a
+ * programmatic dependent of that pass, reduces them into the global scale
+ * fl(2688 / max |x|) (0 -> 1, +inf clamped) in each of its CTAs and quantizes x
+ * as h3q_quantize_nvfp4 does with that scale.  Outputs: codes, scales and the
+ * global scale used (a device fp32 scalar written here).
  *
  * Limit: a shape whose abs-max pass needs more than 4,096 partial maxima (CTAs)
  * is rejected with H3Q_ERR_INVALID_ARGUMENT; on one GPU the pass launches at

@@ -72,6 +72,10 @@ __device__ __align__(256) float g_partial_amax[kMaxDynamicPartials];
 __global__ void __launch_bounds__(kThreads)
 amax_partials_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
                      float* __restrict__ partial) {
+  // the quantize launched after this pass (programmatic dependent launch) may start
+  // as this grid's CTAs finish; it waits for the grid's completion before it
+  // reads the partial maxima
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float scratch[32];
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
@@ -108,24 +112,6 @@ amax_partials_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, i
   }
 }
 
-// One CTA: the maximum of n partial maxima, then the global scale from it.
-__global__ void __launch_bounds__(256)
-scale_from_partials_kernel(const float* __restrict__ partial, int n, float* __restrict__ gsf) {
-  __shared__ float scratch[8];
-  float m = 0.0f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partial[i]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float a = 0.0f;
-    for (int w = 0; w < 8; ++w) a = fmaxf(a, scratch[w]);
-    if (a > FLT_MAX) a = FLT_MAX;
-    *gsf = a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
-  }
-}
-
 }  // namespace
 
 cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks) {
@@ -134,8 +120,8 @@ cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks) {
                            (rows * segs + kWarps - 1) / kWarps, blocks);
 }
 
-cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
-                                        int blocks, float* gsf, cudaStream_t stream) {
+cudaError_t launch_dynamic_partials(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols, int blocks,
+                                    const float** partials, cudaStream_t stream) {
   // The device address of the scratch array in the current context.  It is
   // looked up on every call (a lookup, no allocation): a cached address would
   // point into a context the caller may since have destroyed, or into another
@@ -145,9 +131,7 @@ cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t r
   if (err != cudaSuccess) return err;
   float* partial = static_cast<float*>(address);
   amax_partials_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, partial);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  scale_from_partials_kernel<<<1, 256, 0, stream>>>(partial, blocks, gsf);
+  *partials = partial;
   return cudaGetLastError();
 }
 

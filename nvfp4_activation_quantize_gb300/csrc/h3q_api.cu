@@ -487,11 +487,11 @@ int h3q_quantize_nvfp4_dynamic(const void* x, int64_t ld_x, int64_t rows, int64_
     return fail(H3Q_ERR_INVALID_ARGUMENT, "%s: the abs-max pass needs %d partial maxima, more than "
                 "the %d the static scratch holds", fn, blocks, h3q::kMaxDynamicPartials);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  err = h3q::launch_dynamic_scale_static(static_cast<const uint16_t*>(x), ld_x, rows, cols, blocks,
-                                         global_scale, st);
+  const float* partials = nullptr;
+  err = h3q::launch_dynamic_partials(static_cast<const uint16_t*>(x), ld_x, rows, cols, blocks, &partials, st);
   if (err != cudaSuccess) return cuda_failed(fn, err);
-  err = h3q::launch_quantize(static_cast<const uint16_t*>(x), ld_x, rows, cols, global_scale, codes,
-                             scales, st);
+  err = h3q::launch_quantize_after_partials(static_cast<const uint16_t*>(x), ld_x, rows, cols, partials, blocks,
+                                            global_scale, codes, scales, st);
   return err == cudaSuccess ? H3Q_OK : cuda_failed(fn, err);
 }
 

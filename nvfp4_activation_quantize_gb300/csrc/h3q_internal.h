@@ -56,11 +56,17 @@ cudaError_t launch_global_scale(const float* amax, float* gsf, cudaStream_t stre
 // Dynamic quantize without caller scratch: per-CTA partial maxima in a
 // file-scope device array of kMaxDynamicPartials floats.  dynamic_scale_partials
 // gives the number of CTAs (partials) the abs-max pass launches for a shape;
-// launch_dynamic_scale_static runs that pass and writes the global scale.
+// launch_dynamic_partials runs that pass (and returns the array's address);
+// launch_quantize_after_partials then quantizes with the scale it forms from the
+// partial maxima (written to gsf_out too), launched as a programmatic dependent of
+// the pass.
 constexpr int kMaxDynamicPartials = 4096;
 cudaError_t dynamic_scale_partials(int64_t rows, int64_t cols, int* blocks);
-cudaError_t launch_dynamic_scale_static(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
-                                        int blocks, float* gsf, cudaStream_t stream);
+cudaError_t launch_dynamic_partials(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols, int blocks,
+                                    const float** partials, cudaStream_t stream);
+cudaError_t launch_quantize_after_partials(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
+                                           const float* partials, int n_partials, float* gsf_out,
+                                           uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
 // Residual fold + RMSNorm + AdaLN -> NVFP4 (rows of at most 8,192 columns).
 cudaError_t launch_residual_adaln(float* h, int64_t ld_h, const uint16_t* o, int64_t ld_o,
