@@ -30,20 +30,23 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 2;  // segments per step (a step's loads, then the previous step's conversions)
 
-// partials: the dynamic form.  The global scale is not read but formed here from
-// the n_partials per-CTA maxima of the abs-max pass launched just before, whose
-// completion this kernel waits for (programmatic dependent launch: its CTAs start
-// as the pass's CTAs finish and issue their first loads of x, which the pass does
-// not write, before the wait); the first CTA also writes the scale to gsf_out.
-// The scale is the one h3q_global_scale_from_amax forms: fl(2688 / max), 1 for 0,
-// +inf clamped to the largest finite binary32 first.
-__global__ void __launch_bounds__(kThreads)
-quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
-                const float* __restrict__ gsf_ptr, uint8_t* __restrict__ codes,
-                uint8_t* __restrict__ scales, const float* __restrict__ partials, int n_partials,
-                float* __restrict__ gsf_out) {
+// The quantize of x, persistent over (row, 512-column segment) units.  DYN: the
+// dynamic form.  The global scale is not read but formed here from the
+// n_partials per-CTA maxima of the abs-max pass launched just before, whose
+// completion this waits for (programmatic dependent launch: the CTAs start as the
+// pass's CTAs finish and issue their first loads of x, which the pass does not
+// write, before the wait); the first CTA also writes the scale to gsf_out.  The
+// scale is the one h3q_global_scale_from_amax forms: fl(2688 / max), 1 for 0,
+// +inf clamped to the largest finite binary32 first.  Each form has a kernel of
+// its own, so the static one keeps its parameters and registers (63: four CTAs
+// of 256 threads per SM; the dynamic one takes 64).
+template <bool DYN>
+__device__ __forceinline__ void quantize_rows(const uint16_t* __restrict__ x, int64_t ld, int64_t rows,
+                                              int64_t cols, const float* __restrict__ gsf_ptr,
+                                              uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                              const float* __restrict__ partials, int n_partials,
+                                              float* __restrict__ gsf_out) {
   __shared__ float inv_table[128];
-  __shared__ float scratch[kWarps];
 
   const int lane = threadIdx.x & 31;
   const int64_t groups = cols >> 4;
@@ -79,24 +82,27 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_
     }
   };
   load_step(in, row, seg);  // the first loads are in flight during the prologue
-  float gsf;
-  if (partials != nullptr) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the abs-max pass has completed
-    float m = 0.0f;
-    for (int i = threadIdx.x; i < n_partials; i += kThreads) m = fmaxf(m, partials[i]);
+  const float gsf = [&]() -> float {
+    if constexpr (DYN) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the abs-max pass has completed
+      __shared__ float scratch[kWarps];
+      float m = 0.0f;
+      for (int i = threadIdx.x; i < n_partials; i += kThreads) m = fmaxf(m, partials[i]);
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) scratch[threadIdx.x >> 5] = m;
-    __syncthreads();
-    float a = 0.0f;
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) scratch[threadIdx.x >> 5] = m;
+      __syncthreads();
+      float a = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) a = fmaxf(a, scratch[w]);
-    if (a > FLT_MAX) a = FLT_MAX;
-    gsf = a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *gsf_out = gsf;
-  } else {
-    gsf = *gsf_ptr;
-  }
+      for (int w = 0; w < kWarps; ++w) a = fmaxf(a, scratch[w]);
+      if (a > FLT_MAX) a = FLT_MAX;
+      const float g = a == 0.0f ? 1.0f : __fdiv_rn(2688.0f, a);
+      if (blockIdx.x == 0 && threadIdx.x == 0) *gsf_out = g;
+      return g;
+    } else {
+      return *gsf_ptr;
+    }
+  }();
   fill_inverse_scales(inv_table, gsf);
   __syncthreads();
   while (row[0] < prows) {
@@ -133,6 +139,21 @@ quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_
   }
 }
 
+
+__global__ void __launch_bounds__(kThreads)
+quantize_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
+                const float* __restrict__ gsf_ptr, uint8_t* __restrict__ codes,
+                uint8_t* __restrict__ scales) {
+  quantize_rows<false>(x, ld, rows, cols, gsf_ptr, codes, scales, nullptr, 0, nullptr);
+}
+
+__global__ void __launch_bounds__(kThreads)
+quantize_dynamic_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
+                        const float* __restrict__ partials, int n_partials, float* __restrict__ gsf_out,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  quantize_rows<true>(x, ld, rows, cols, nullptr, codes, scales, partials, n_partials, gsf_out);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t ld, int64_t rows, int64_t cols,
@@ -144,7 +165,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t ld, int64_t rows, int64_t
   cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&quantize_kernel), kThreads, 0,
                                       (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
-  quantize_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, gsf, codes, scales, nullptr, 0, nullptr);
+  quantize_kernel<<<blocks, kThreads, 0, stream>>>(x, ld, rows, cols, gsf, codes, scales);
   return cudaGetLastError();
 }
 
@@ -154,7 +175,7 @@ cudaError_t launch_quantize_after_partials(const uint16_t* x, int64_t ld, int64_
   const int64_t segs = (cols / 16 + 31) / 32;
   const int64_t work = (rows + 127) / 128 * 128 * segs;
   int blocks = 0;
-  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&quantize_kernel), kThreads, 0,
+  cudaError_t err = persistent_blocks(reinterpret_cast<const void*>(&quantize_dynamic_kernel), kThreads, 0,
                                       (work + kWarps - 1) / kWarps, &blocks);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -167,8 +188,8 @@ cudaError_t launch_quantize_after_partials(const uint16_t* x, int64_t ld, int64_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel, x, ld, rows, cols, static_cast<const float*>(nullptr), codes,
-                            scales, partials, n_partials, gsf_out);
+  return cudaLaunchKernelEx(&cfg, quantize_dynamic_kernel, x, ld, rows, cols, partials, n_partials, gsf_out, codes,
+                            scales);
 }
 
 }  // namespace h3q
