@@ -542,7 +542,7 @@ def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
             step()
     torch.cuda.synchronize()
     steps = max(3, min(args.steps, 10))
-    total_ms, _ = time_launches(step, steps, stream)
+    total_ms, per_step = time_launches(step, steps, stream)
     total_ms = max_over_ranks(total_ms, world, dev)
     nbytes = adaln_bytes(ROWS, COLS, FRAMES)
     h2d = hx.numel() * 2 + hg.numel() * 2 + ht.numel() * 2
@@ -565,6 +565,52 @@ def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
         out["host_link"] = dict(link, bound_ms_per_step=round(bound, 3),
                                 frac_of_link_bound=round(bound / (total_ms / steps), 3),
                                 step_buffers=buffer_rates(dev, hx, hc))
+        out["step_ms"] = [round(v, 3) for v in per_step]
+        out["chunk_copies"] = chunk_copies(dev, hx, hc, hs, pipe.chunk_rows)
+    return out
+
+
+def chunk_copies(dev, hx, hc, hs, chunk_rows: int) -> dict:
+    """The step's own copies without the producer: x host to device chunk by chunk
+    on one stream, codes and scales device to host chunk by chunk on another, each
+    direction alone and both at once (ms for the whole step's bytes).  Set beside
+    the pipelined step's time, it tells a slow step whose copies are slow from one
+    whose copies are fine but badly overlapped."""
+    rows, quads = hx.shape[0], hx.shape[1] // 64
+    dx = torch.empty((chunk_rows, hx.shape[1]), dtype=hx.dtype, device=dev)
+    dc = torch.empty((chunk_rows, hc.shape[1]), dtype=hc.dtype, device=dev)
+    ds = torch.empty(chunk_rows * hs.shape[1], dtype=hs.dtype, device=dev)
+    hs_flat = hs.view(-1)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            for r0 in range(0, rows, chunk_rows):
+                n = min(chunk_rows, rows - r0)
+                dx[:n].copy_(hx[r0:r0 + n], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            for r0 in range(0, rows, chunk_rows):
+                n = min(chunk_rows, rows - r0)
+                pad_n = -(-n // 128) * 128
+                hc[r0:r0 + n].copy_(dc[:n], non_blocking=True)
+                o = r0 // 128 * quads * 512
+                hs_flat[o:o + pad_n * hs.shape[1]].copy_(ds[:pad_n * hs.shape[1]], non_blocking=True)
+
+    def timed(*fns, reps=3):
+        res = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for fn in fns:
+                fn()
+            torch.cuda.synchronize()
+            res.append((time.perf_counter() - t0) * 1e3)
+        return round(min(res), 3)
+
+    out = {"h2d_ms": timed(h2d), "d2h_ms": timed(d2h), "both_ms": timed(h2d, d2h)}
+    del dx, dc, ds
     return out
 
 
@@ -742,7 +788,8 @@ def measure_producers(h3q, dev, stream, args):
             dq["two_pass_algorithmic_bytes"] = quantize_bytes(*x.shape) + 2 * x.numel()
             dq["frac_of_peak_two_pass"] = round(dq["two_pass_algorithmic_bytes"] / (dq["median_launch_ms"] * 1e-3)
                                                 / 1e9 / peak, 4)
-            dq["note"] = "abs-max pass + device scale + quantize in one call; GB/s by the single-pass bytes"
+            dq["note"] = ("abs-max pass, then the quantize forming the scale from its partial maxima (a "
+                          "programmatic dependent launch), in one call; GB/s by the single-pass bytes")
             res["attn_out_quantize_dynamic_65280x7168"] = dq
             # the checking-path dequantize of that output: codes + scales in, fp32 out
             out = torch.empty(x.shape, dtype=torch.float32, device=dev)
