@@ -3,7 +3,15 @@ host and launches on the caller's stream (no allocation, no synchronisation),
 so a step of the AdaLN, SwiGLU, quantize, residual-fold, QKV-epilogue and
 dynamic-scale calls captures into one graph.  Replays produce the same bytes as
 eager calls, and replaying after the inputs change in place recomputes from the
-new inputs."""
+new inputs.  The no-scratch dynamic quantize launches its quantize as a
+programmatic dependent of the abs-max pass; captured, that becomes a graph edge,
+also when the call is the process's first of it (its per-device lookups then
+happen during the capture)."""
+import os
+import subprocess
+import sys
+import textwrap
+
 import pytest
 import torch
 
@@ -40,6 +48,8 @@ def _step(w, outs, stream):
     h3q.h3q_global_scale_from_amax(outs["amax"], outs["dyn_gsf"], stream=stream)
     h3q.h3q_rmsnorm_adaln_nvfp4(d["x"], d["gamma"], d["table"], outs["dyn_gsf"], rows_per_frame=d["rows_per_frame"],
                                 eps=d["eps"], codes=outs["d_codes"], scales=outs["d_scales"], stream=stream)
+    h3q.h3q_quantize_nvfp4_dynamic(w["attn"], global_scale=outs["qd_gsf"], codes=outs["qd_codes"],
+                                   scales=outs["qd_scales"], stream=stream)
 
 
 def _buffers(w, dev):
@@ -53,6 +63,8 @@ def _buffers(w, dev):
     outs["q_codes"], outs["q_scales"] = nv(*w["attn"].shape)
     outs["r_codes"], outs["r_scales"] = nv(*w["residual"]["o"].shape)
     outs["d_codes"], outs["d_scales"] = nv(*w["dyn"]["x"].shape)
+    outs["qd_codes"], outs["qd_scales"] = nv(*w["attn"].shape)
+    outs["qd_gsf"] = torch.zeros(1, dtype=torch.float32, device=dev)
     outs["h"] = torch.empty_like(w["residual"]["h"])
     q = w["qkv"]
     for name in ("qo", "ko", "vo"):
@@ -95,5 +107,41 @@ def test_producers_in_a_captured_graph(dev):
     with torch.cuda.stream(side):
         _step(w, eager, side)
     torch.cuda.synchronize()
-    for k in ("q_codes", "q_scales", "d_codes", "d_scales", "dyn_gsf"):
+    for k in ("q_codes", "q_scales", "d_codes", "d_scales", "dyn_gsf", "qd_codes", "qd_scales", "qd_gsf"):
         assert torch.equal(outs[k].view(torch.uint8), eager[k].view(torch.uint8)), f"replay after update: {k}"
+
+
+_FIRST_CALL_CAPTURED = textwrap.dedent("""
+    import torch
+    import nvfp4_activation_quantize_gb300 as h3q
+    import workloads
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    x = workloads.attention_output(dev, tokens=1000, seed=47)
+    codes = torch.empty((1000, x.shape[1] // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((h3q.padded_rows(1000), x.shape[1] // 16), dtype=torch.uint8, device=dev)
+    gsf = torch.zeros(1, dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):  # the process's first call of the entry point
+        h3q.h3q_quantize_nvfp4_dynamic(x, global_scale=gsf, codes=codes, scales=scales, stream=side)
+    graph.replay()
+    torch.cuda.synchronize()
+    c, s, g = h3q.h3q_quantize_nvfp4_dynamic(x)
+    torch.cuda.synchronize()
+    assert torch.equal(codes, c) and torch.equal(scales, s) and torch.equal(gsf, g), "replay differs"
+    x.mul_(0.25)
+    graph.replay()
+    c, s, g = h3q.h3q_quantize_nvfp4_dynamic(x)
+    torch.cuda.synchronize()
+    assert torch.equal(codes, c) and torch.equal(scales, s) and torch.equal(gsf, g), "replay after update"
+    print("ok")
+""")
+
+
+def test_dynamic_quantize_first_called_inside_a_capture(dev):
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([root, os.path.join(root, "tests")]))
+    res = subprocess.run([sys.executable, "-c", _FIRST_CALL_CAPTURED], cwd=root, env=env, capture_output=True,
+                         text=True, timeout=600)
+    assert res.returncode == 0 and res.stdout.strip().endswith("ok"), res.stdout[-2000:] + res.stderr[-2000:]
