@@ -57,7 +57,9 @@ def _check(dev, w, frames, gsf, codes, scales, rstd, h_after, what):
 @pytest.mark.parametrize("rows,cols,frames_n,rpf,with_bias", [
     (1, 64, 1, 1, True), (130, 256, 3, 50, True), (257, 1024, 2, 200, False), (100, 2048, 4, 25, True),
     (300, 4096, 2, 150, True), (457, 7168, 3, 160, True), (64, 8192, 1, 64, False),
-    (33, 1088, 4, 9, True), (99, 2560, 2, 50, False)])
+    (33, 1088, 4, 9, True), (99, 2560, 2, 50, False),
+    # the 7,168-column ring kernel: one row per CTA, no bias, frames changing inside a CTA's rows
+    (1, 7168, 1, 1, False), (5, 7168, 2, 3, True), (151, 7168, 2, 100, False), (1000, 7168, 4, 300, True)])
 def test_shapes(dev, rows, cols, frames_n, rpf, with_bias):
     w = workloads.residual_inputs(dev, rows=rows, cols=cols, frames=frames_n, rows_per_frame=rpf,
                                   seed=rows + cols, bias=with_bias)
