@@ -645,15 +645,18 @@ def host_link(dev, nbytes: int = 512 << 20, reps: int = 8) -> dict:
     d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def timed(fn):
+    def timed(fn, trials: int = 3):
         for _ in range(2):
             fn()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            fn()
-        torch.cuda.synchronize()
-        return reps * nbytes / (time.perf_counter() - t0) / 1e9
+        rates = []
+        for _ in range(trials):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+            rates.append(round(reps * nbytes / (time.perf_counter() - t0) / 1e9, 1))
+        return rates
 
     def both():
         with torch.cuda.stream(s1):
@@ -661,9 +664,14 @@ def host_link(dev, nbytes: int = 512 << 20, reps: int = 8) -> dict:
         with torch.cuda.stream(s2):
             h_out.copy_(d_out, non_blocking=True)
 
-    res = {"h2d_gbs": round(timed(lambda: d_in.copy_(h_in, non_blocking=True)), 1),
-           "d2h_gbs": round(timed(lambda: h_out.copy_(d_out, non_blocking=True)), 1),
-           "both_gbs_each": round(timed(both), 1), "bytes_per_copy": nbytes}
+    # each rate is the best of three trials (the link's capability); the two-way
+    # trials are kept, since concurrent copies in both directions now and then run
+    # at about half their usual rate on this platform
+    h2d = timed(lambda: d_in.copy_(h_in, non_blocking=True))
+    d2h = timed(lambda: h_out.copy_(d_out, non_blocking=True))
+    two = timed(both)
+    res = {"h2d_gbs": max(h2d), "d2h_gbs": max(d2h), "both_gbs_each": max(two), "both_gbs_trials": two,
+           "bytes_per_copy": nbytes}
     del h_in, h_out, d_in, d_out
     return res
 
