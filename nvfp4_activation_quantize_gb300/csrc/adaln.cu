@@ -96,6 +96,15 @@ struct FrameCursor {
     }
     return clamp_frame(a, frame);
   }
+  // the same for decreasing rows: next - rows_per_frame is the frame's first row
+  __device__ __forceinline__ int64_t at_down(const AdalnArgs& a, int64_t row) {
+    if (a.row_frame) return clamp_frame(a, a.row_frame[row]);
+    while (row < next - a.rows_per_frame) {
+      --frame;
+      next -= a.rows_per_frame;
+    }
+    return clamp_frame(a, frame);
+  }
 };
 
 // gamma and 1 + scale of chunk c of frame t as fp32 pairs (elements 2i, 2i+1)
@@ -617,9 +626,16 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   const int steps = static_cast<int>((r_end - r_begin + R - 1) / R);
   const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
+  // The abs-max pass takes the rows of its range from the end to the start (row
+  // r_end - 1 - i where the producer takes r_begin + i): the producer that
+  // follows starts each range at its first rows, the last ones this pass read,
+  // part of them still in L2 (a maximum and a row's rstd do not depend on the
+  // order).
+  constexpr bool kReverse = AMAX;
+
   // pass-1 lanes: the next row to copy and its ring slot
-  const uint16_t* x_next = a.x + (r_begin + grp) * a.ld + l * 8;
-  const int64_t x_step = R * a.ld;
+  const uint16_t* x_next = kReverse ? a.x + (r_end - 1 - grp) * a.ld + l * 8 : a.x + (r_begin + grp) * a.ld + l * 8;
+  const int64_t x_step = kReverse ? -R * a.ld : R * a.ld;
   const int l_slot = l ^ ((l >> 3) & 1);  // chunk c at slot c ^ ((c >> 3) & 1): conflict-free in both passes
   const uint32_t ring_l = ring_base + static_cast<uint32_t>(grp * kChunks + l_slot) * 16;
   // a step's ring stage is its index mod kStages, kept by a wrapping counter
@@ -653,7 +669,7 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   };
   // the stats warp: lane k < R publishes row k of step q.  GIVEN: the rstd is read
   // a step ahead of its publication, so the load is off the publishing chain.
-  FrameCursor lane_cursor(a, r_begin + (lane < R ? lane : 0));
+  FrameCursor lane_cursor(a, kReverse ? (r_end > r_begin ? r_end - 1 : r_begin) : r_begin + (lane < R ? lane : 0));
   float given = 0.0f;
   auto fetch_given = [&](int q) {
     const int64_t r = r_begin + R * int64_t{q} + lane;
@@ -662,7 +678,8 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
   fetch_given(0);
   auto stats = [&](int q) {
     if (q >= steps || lane >= R) return;
-    const int64_t r = r_begin + R * int64_t{q} + lane;
+    const int64_t r = kReverse ? r_end - 1 - (R * int64_t{q} + lane) : r_begin + R * int64_t{q} + lane;
+    const bool valid = kReverse ? r >= r_begin : r < r_end;
     const float* T = totals[q & 1][lane];
     RowInfo info;
     if (GIVEN) {
@@ -671,10 +688,10 @@ __global__ void __launch_bounds__(NB, 1) adaln_block_kernel(const AdalnArgs a) {
     } else {
       info.rstd = rstd_of(__fadd_rn(__fadd_rn(T[0], T[1]), __fadd_rn(T[2], T[3])), cols_f, a.eps);
     }
-    info.frame = r < r_end ? static_cast<int32_t>(lane_cursor.at(a, r)) : -1;
+    info.frame = valid ? static_cast<int32_t>(kReverse ? lane_cursor.at_down(a, r) : lane_cursor.at(a, r)) : -1;
     info.scale_off = scale_row_offset(r, quads);
     rows_s[q & 1][lane] = info;
-    if (a.row_rstd != nullptr && r < r_end) a.row_rstd[r] = info.rstd;
+    if (a.row_rstd != nullptr && valid) a.row_rstd[r] = info.rstd;
   };
 
   ChunkTables tb[2];
