@@ -521,7 +521,7 @@ def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
     """The same metric through the C-ABI host-buffer call (h3q_rmsnorm_adaln_nvfp4_host,
     through HostPipeline): each step copies gamma and the modulation table from pinned
     host memory to the device, then the call copies x in, runs the producer and copies
-    codes and scales back to pinned host memory, pipelined over 8,192-row chunks (the
+    codes and scales back to pinned host memory, pipelined over 2,048-row chunks (the
     producer on the caller's stream, a library stream per copy direction).  The timed
     region (CUDA events on the caller's stream) covers every copy of the step."""
     from nvfp4_activation_quantize_gb300.host import HostPipeline
@@ -532,7 +532,7 @@ def measure_e2e_placed(h3q, dev, stream, w, gsf, args, world=1):
     ht = w["table"].cpu().pin_memory()
     hc = torch.empty((ROWS, COLS // 2), dtype=torch.uint8).pin_memory()
     hs = torch.empty((padded(ROWS), COLS // 16), dtype=torch.uint8).pin_memory()
-    pipe = HostPipeline(dev, COLS, chunk_rows=8192)
+    pipe = HostPipeline(dev, COLS, chunk_rows=2048)
 
     def step():
         pipe.rmsnorm_adaln_nvfp4(hx, hg, ht, gsf, hc, hs, rows_per_frame=RPF, eps=w["eps"])

@@ -34,7 +34,7 @@ class HostPipeline:
 
     depth = 3  # the library's staging slots
 
-    def __init__(self, device, max_cols: int, chunk_rows: int = 8192):
+    def __init__(self, device, max_cols: int, chunk_rows: int = 2048):
         if chunk_rows <= 0 or chunk_rows % 128:
             raise ValueError("chunk_rows must be a positive multiple of 128")
         self.device = torch.device(device)
