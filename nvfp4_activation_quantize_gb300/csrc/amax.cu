@@ -22,10 +22,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
 
-// Warp per 512-column segment, lane per 16-element block, as in the quantize, the
-// segments taken from the end of x to its start: a quantize of x that follows
-// then starts on rows this pass read last, part of them still in L2 (a maximum
-// does not depend on the order).
+// Warp per 512-column segment, lane per 16-element block, as in the quantize.
 __global__ void __launch_bounds__(kThreads)
 amax_bf16_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
                  float* __restrict__ amax) {
@@ -42,9 +39,8 @@ amax_bf16_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t s = s0 + u * nwarps;
-      const int64_t sr = total - 1 - s;  // units in reverse order
-      const int64_t row = sr / segs;
-      const int64_t g = (sr - row * segs) * 32 + lane;
+      const int64_t row = s / segs;
+      const int64_t g = (s - row * segs) * 32 + lane;
       if (s < total && g < groups) {
         load_stream(x + row * ld + g * kBlock, in[u]);
       } else {
@@ -72,9 +68,7 @@ __global__ void global_scale_kernel(const float* __restrict__ amax, float* __res
 __device__ __align__(256) float g_partial_amax[kMaxDynamicPartials];
 
 // Each CTA writes its own max |x| to partial[blockIdx.x] (no atomics, nothing to
-// zero beforehand).  The pass walks x from its end to its start, so that when the
-// quantize that follows starts at the first rows they are the last ones this pass
-// read, and part of them is still in L2 (a maximum does not depend on the order).
+// zero beforehand).
 __global__ void __launch_bounds__(kThreads)
 amax_partials_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, int64_t cols,
                      float* __restrict__ partial) {
@@ -95,9 +89,8 @@ amax_partials_kernel(const uint16_t* __restrict__ x, int64_t ld, int64_t rows, i
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t s = s0 + u * nwarps;
-      const int64_t sr = total - 1 - s;  // units in reverse order
-      const int64_t row = sr / segs;
-      const int64_t g = (sr - row * segs) * 32 + lane;
+      const int64_t row = s / segs;
+      const int64_t g = (s - row * segs) * 32 + lane;
       if (s < total && g < groups) {
         load_stream(x + row * ld + g * kBlock, in[u]);
       } else {
