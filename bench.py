@@ -901,16 +901,14 @@ def measure_producers(h3q, dev, stream, args):
     x = workloads.quantize_inputs(dev)
     g = torch.tensor([2688.0 / float(x.float().abs().max())], dtype=torch.float32, device=dev)
     c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
-    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream,
-                           flush=lambda: scrub.fill_(1))
+                           flush=lambda: l2_scrub.fill_(1))
     res["quantize_8192x7168_l2_flushed"] = entry(quantize_bytes(*x.shape), per, 8192)
     # The write leaves L2 full of dirty lines, whose write-back then falls inside the timed launch.
-    # Reading a second 2 x L2 buffer after it writes them back first: the launch starts on an L2
-    # of clean lines that hold none of its inputs.
-    clean = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    # Reading a second 2 x L2 buffer after it (l2_flush) writes them back first: the launch starts
+    # on an L2 of clean lines that hold none of its inputs.
     _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream,
-                           flush=lambda: (scrub.fill_(1), clean.sum()))
+                           flush=l2_flush)
     res["quantize_8192x7168_l2_flushed_clean"] = entry(quantize_bytes(*x.shape), per, 8192)
     del x, c, s
 
@@ -938,24 +936,20 @@ def measure_producers(h3q, dev, stream, args):
     # their time, so they measure latency, not bandwidth.
     #  - the tiny AdaLN case (64 x 256);
     #  - the ragged attention-output quantize at 1,000 tokens (18 MB).
-    def flush():
-        scrub.fill_(1)
-        clean.sum()
-
     w = workloads.tiny_adaln_inputs(dev)
     g = torch.tensor([calibrate_adaln_gsf(w)], dtype=torch.float32, device=dev)
     c, s = h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], g, rows_per_frame=w["rows_per_frame"],
                                        eps=w["eps"], stream=stream)
     _, per = time_launches(lambda: h3q.h3q_rmsnorm_adaln_nvfp4(
         w["x"], w["gamma"], w["table"], g, rows_per_frame=w["rows_per_frame"], eps=w["eps"], codes=c,
-        scales=s, stream=stream), n, stream, flush=flush)
+        scales=s, stream=stream), n, stream, flush=l2_flush)
     res["adaln_tiny_64x256_l2_flushed_clean"] = entry(adaln_bytes(64, 256, w["table"].shape[0]), per, 64)
     x = workloads.attention_output(dev, tokens=1000)
     g = torch.tensor([2688.0 / float(x.abs().max().float())], dtype=torch.float32, device=dev)
     c, s = h3q.h3q_quantize_nvfp4(x, g, stream=stream)
-    _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream, flush=flush)
+    _, per = time_launches(lambda: h3q.h3q_quantize_nvfp4(x, g, c, s, stream=stream), n, stream, flush=l2_flush)
     res["attn_out_quantize_1000x7168_l2_flushed_clean"] = entry(quantize_bytes(*x.shape), per, 1000)
-    del w, x, c, s, scrub, clean
+    del w, x, c, s, l2_scrub, l2_clean
     torch.cuda.empty_cache()
     if not args.no_cpu_baseline:
         for key, kind in (("swiglu_65280x18944", "swiglu"), ("swiglu_packed_bias_65280x18944", "swiglu_packed"),
