@@ -169,6 +169,33 @@ def test_dynamic_adaln_65280x7168_every_row(dev):
     check_full(codes2, scales2, rows, cols, co, so, "dynamic adaln from rstd 65280x7168")
 
 
+def test_adaln_7168_short_frames(dev):
+    """The 7,168-column block kernel with two rows per frame and about 30 rows per
+    CTA: each lane's rows three apart cross one or two frame boundaries a step, in
+    the abs-max pass (which takes its rows downwards) and in both producers.  The
+    pass's maximum and rstd, and the codes and scales of the producer forming its
+    own statistics and of the one given the rstd, against the oracle."""
+    rows, cols, rpf = 4561, 7168, 2
+    w = workloads.adaln_inputs(dev, rows=rows, cols=cols, frames=(rows + rpf - 1) // rpf, rows_per_frame=rpf,
+                               seed=77)
+    frames = np.arange(rows) // rpf
+    rstd = torch.empty(rows, dtype=torch.float32, device=dev)
+    amax = h3q.h3q_rmsnorm_adaln_amax(w["x"], w["gamma"], w["table"], rows_per_frame=rpf, eps=w["eps"],
+                                      row_rstd=rstd)
+    gsf = h3q.h3q_global_scale_from_amax(amax)
+    c1, s1 = h3q.h3q_rmsnorm_adaln_nvfp4_from_rstd(w["x"], w["gamma"], w["table"], rstd, gsf, rows_per_frame=rpf)
+    c2, s2 = h3q.h3q_rmsnorm_adaln_nvfp4(w["x"], w["gamma"], w["table"], gsf, rows_per_frame=rpf, eps=w["eps"])
+    _, _, _, y = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                   None, want_y=True, threads=THREADS)
+    _eq(amax, oracle.amax_bf16(y), "adaln amax short frames")
+    g = oracle.global_scale_from_amax(oracle.amax_bf16(y))
+    co, so, rstd_o, _ = oracle.adaln_rows(bits(w["x"]), bits(w["gamma"]), bits(w["table"]), frames, w["eps"],
+                                          g, threads=THREADS)
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), rstd_o.view(np.uint32)), "abs-max pass rstd"
+    check_full(c1, s1, rows, cols, co, so, "adaln from rstd, short frames")
+    check_full(c2, s2, rows, cols, co, so, "adaln, short frames")
+
+
 @pytest.mark.parametrize("rows,cols,use_row_frame", [(5, 64, False), (130, 256, True), (257, 1024, False),
                                                      (100, 2048, True), (1, 7168, False), (4, 7168, True),
                                                      (457, 7168, False), (458, 7168, True), (64, 8192, False),
